@@ -1,0 +1,396 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself
+(brute force, library routines, closed forms, the pages' printed numbers)."""
+import itertools
+import json
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ route
+def brute_topk(l, k):
+    """Enumerate every k-subset; keep the one that dominates all left-out experts
+    (strictly larger logit, or equal logit and a lower index)."""
+    E = len(l)
+    winners = []
+    for S in itertools.combinations(range(E), k):
+        rest = [j for j in range(E) if j not in S]
+        if all(l[i] > l[j] or (l[i] == l[j] and i < j) for i in S for j in rest):
+            winners.append(set(S))
+    assert len(winners) == 1
+    return winners[0]
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (4, 2), (6, 3), (8, 2), (8, 8), (10, 4)])
+def test_route_brute_force_with_ties(E, k):
+    rng = np.random.default_rng(E * 31 + k)
+    for trial in range(40):
+        # small integer-valued logits force many ties; signed zeros must tie too
+        l = rng.integers(-2, 3, size=(1, E)).astype(np.float32)
+        if trial % 3 == 0:
+            l[0, rng.integers(0, E)] = -0.0
+        ids, w = O.route(l, k)
+        assert set(ids[0].tolist()) == brute_topk(l[0].tolist(), k)
+        sel = l[0][ids[0]]
+        # the chosen order: logit descending, then index ascending
+        for a in range(k - 1):
+            assert sel[a] > sel[a + 1] or (sel[a] == sel[a + 1] and ids[0][a] < ids[0][a + 1])
+        assert abs(w.sum() - 1.0) < 1e-12
+
+
+def test_route_signed_zero_is_a_tie():
+    l = np.array([[-0.0, 0.0, -1.0]], dtype=np.float32)
+    ids, _ = O.route(l, 1)
+    assert ids[0, 0] == 0
+
+
+def test_route_k_equals_E_is_softmax():
+    rng = np.random.default_rng(1)
+    l = rng.standard_normal((16, 8)).astype(np.float32)
+    ids, w = O.route(l, 8)
+    ref = torch.softmax(torch.from_numpy(l).double(), dim=1).numpy()
+    got = np.zeros_like(ref)
+    np.put_along_axis(got, ids.astype(np.int64), w, axis=1)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-14)
+
+
+def test_route_k1_is_argmax_weight_one():
+    rng = np.random.default_rng(2)
+    l = rng.standard_normal((64, 16)).astype(np.float32)
+    ids, w = O.route(l, 1)
+    assert np.array_equal(ids[:, 0], torch.argmax(torch.from_numpy(l), dim=1).numpy())
+    assert np.all(w == 1.0)
+
+
+def test_route_weights_two_forms_agree():
+    l = mi.make_logits(mi.config(0))
+    _, w1 = O.route(l, 2)
+    _, w2 = O.route_softmax_then_renorm(l, 2)
+    np.testing.assert_allclose(w1, w2, rtol=0, atol=1e-12)
+
+
+def test_route_rejects_non_finite():
+    l = np.zeros((2, 4), dtype=np.float32)
+    l[1, 2] = np.nan
+    with pytest.raises(ValueError):
+        O.route(l, 2)
+
+
+# ------------------------------------------------------------------ layout
+def brute_layout(ids, E, phys_of):
+    T, k = ids.shape
+    items = [(phys_of(t, int(ids[t, j])), t, j) for t in range(T) for j in range(k)]
+    items_sorted = sorted(items, key=lambda a: (a[0], a[1]))
+    row_to_token = [t for _, t, _ in items_sorted]
+    slot_to_row = np.zeros((T, k), dtype=np.int64)
+    for r, (_, t, j) in enumerate(items_sorted):
+        slot_to_row[t, j] = r
+    return row_to_token, slot_to_row
+
+
+@pytest.mark.parametrize("T,E,k,R", [(1, 1, 1, 1), (3, 8, 2, 4), (64, 8, 2, 4), (257, 16, 4, 8)])
+def test_layout_brute_force(T, E, k, R):
+    l = np.random.default_rng(T + E).standard_normal((T, E)).astype(np.float32)
+    ids, _ = O.route(l, k)
+    lay = O.dispatch_layout(ids, E, R)
+    r2t, s2r = brute_layout(ids, E, lambda t, e: e)
+    assert lay["row_to_token"].tolist() == r2t
+    assert np.array_equal(lay["slot_to_row"], s2r)
+    cnt = [sum(1 for t in range(T) for j in range(k) if ids[t, j] == e) for e in range(E)]
+    assert lay["phys_counts"].tolist() == cnt
+    assert lay["phys_offsets"][-1] == T * k
+    assert np.array_equal(np.diff(lay["phys_offsets"]), lay["phys_counts"])
+    per = E // R
+    assert lay["rank_counts"].tolist() == [sum(cnt[r * per:(r + 1) * per]) for r in range(R)]
+
+
+def test_dispatch_figure_example():
+    g = load("dispatch_figure.json")
+    # 16 tokens (4 GPUs x 4), top-2 over 8 experts, 2 experts per GPU
+    pairs = [(0, 1)] * 6 + [(6, 7)] * 2 + [(2, 4)] * 4 + [(3, 5)] * 4
+    ids = np.array(pairs, dtype=np.int32)
+    assert ids.shape == (g["gpus"] * g["tokens_per_gpu"], g["top_k"])
+    lay = O.dispatch_layout(ids, g["experts"], g["ep"])
+    assert lay["rank_counts"][0] == g["copies_gpu0"]
+    assert lay["rank_counts"][3] == g["copies_gpu3"]
+    st = lay["stats_after"]
+    assert st["mean_rank"] == 8
+    assert st["max_over_mean"] == pytest.approx(1.5)
+    assert st["balancedness"] == pytest.approx(2 / 3)
+
+
+def page_simulation_counts(setup):
+    """The page's imbalance simulation (section 5.2), restated: expert popularity
+    1/(i+1)^0.4 shuffled with Python's seeded generator, each of 4096 tokens draws
+    distinct experts by weighted choice until it has 8.  The same calls in the same
+    order give the same random stream, which the printed hottest/coldest verify."""
+    rnd = random.Random(setup["python_random_seed"])
+    E, K, T = setup["experts"], setup["top_k"], setup["tokens"]
+    pop = [1 / (i + 1) ** setup["skew"] for i in range(E)]
+    rnd.shuffle(pop)
+    cum = list(itertools.accumulate(pop))
+    counts = [0] * E
+    for _ in range(T):
+        chosen = set()
+        while len(chosen) < K:
+            chosen.add(rnd.choices(range(E), cum_weights=cum)[0])
+        for e in chosen:
+            counts[e] += 1
+    return np.array(counts)
+
+
+@pytest.fixture(scope="module")
+def sim():
+    g = load("imbalance_sim_table.json")
+    return g, page_simulation_counts(g["setup"])
+
+
+def test_sim_reproduces_printed_extremes(sim):
+    g, counts = sim
+    assert counts.max() == g["hottest"] and counts.min() == g["coldest"]
+    assert round(counts.sum() / counts.size) == g["average"]
+
+
+def test_sim_contiguous_column(sim):
+    g, counts = sim
+    for row in g["rows"]:
+        st = O.rank_stats(O.linear_rank_counts(counts, row["ep"]), int(counts.sum()))
+        assert round(st["max_over_mean"], 2) == row["contiguous"]
+        assert st["balancedness"] == pytest.approx(1 / st["max_over_mean"])
+
+
+def test_sim_rebalance_columns(sim):
+    g, counts = sim
+    for row in g["rows"]:
+        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
+            load_ = O.greedy_rebalance(counts, row["ep"], n_red)
+            assert round(load_.max() / load_.mean(), 2) == row[col]
+
+
+# ------------------------------------------------------------------ EPLB
+def test_eplb_map_geometry_and_hot_list():
+    rng = np.random.default_rng(5)
+    counts = rng.integers(0, 50, size=256)
+    counts[17] = counts[200] = 1000          # a tie at the top: lower index first
+    m = O.eplb_map(counts, 32, 32)
+    g = load("expert_arithmetic.json")
+    assert m["P"] // 32 == g["physical_per_rank_256_32_32"]
+    assert np.bincount(m["phys_rank"], minlength=32).tolist() == [9] * 32
+    hot = m["hot"].tolist()
+    assert hot[0] == 17 and hot[1] == 200
+    # brute force: every hot expert beats every cold one on (count desc, index asc)
+    cold = [e for e in range(256) if e not in hot]
+    for h in hot:
+        for c in cold:
+            assert counts[h] > counts[c] or (counts[h] == counts[c] and h < c)
+    # primaries are the linear blocks; replica j on rank j mod 32
+    for e in range(256):
+        p = m["logical_to_phys"][e, 0]
+        assert m["phys_rank"][p] == e // 8 and m["phys_to_logical"][p] == e
+    for j, e in enumerate(hot):
+        p = m["logical_to_phys"][e, 1]
+        assert m["phys_rank"][p] == j % 32 and m["phys_to_logical"][p] == e
+    assert sorted(m["replica_count"].tolist()).count(2) == 32
+    assert O.eplb_map(counts[:256], 8, 8)["P"] // 8 == g["physical_per_rank_256_8_8"]
+
+
+def test_eplb_token_split_by_parity():
+    cfg = mi.config(3).scaled(T=512)
+    l = mi.make_logits(cfg)
+    ids, _ = O.route(l, cfg.k)
+    m = O.eplb_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.R, cfg.n_redundant)
+    lay = O.dispatch_layout(ids, cfg.E, cfg.R, m)
+    for e in m["hot"][:8]:
+        even = sum(1 for t in range(cfg.T) if e in ids[t] and t % 2 == 0)
+        odd = sum(1 for t in range(cfg.T) if e in ids[t] and t % 2 == 1)
+        assert lay["phys_counts"][m["logical_to_phys"][e, 0]] == even
+        assert lay["phys_counts"][m["logical_to_phys"][e, 1]] == odd
+    r2t, s2r = brute_layout(ids, cfg.E, lambda t, e: int(m["logical_to_phys"][e, t % m["replica_count"][e]]))
+    assert lay["row_to_token"].tolist() == r2t
+    assert np.array_equal(lay["slot_to_row"], s2r)
+
+
+# ------------------------------------------------------------------ number formats
+def test_bf16_rounding_matches_torch():
+    v = np.random.default_rng(3).standard_normal(100000) * 10.0
+    ref = torch.from_numpy(v).float().bfloat16().double().numpy()
+    assert np.array_equal(O.round_bf16(v), ref)
+
+
+def test_e4m3_table_landmarks():
+    assert O.e4m3_value(0x7E) == 448.0
+    assert O.e4m3_value(0x08) == 2.0 ** -6
+    assert O.e4m3_value(0x01) == 2.0 ** -9
+    assert np.isnan(O.e4m3_value(0x7F))
+    assert O.e4m3_encode(np.array([1000.0, -1e9, 448.0], np.float32)).tolist() == [0x7E, 0xFE, 0x7E]
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(4)
+    v = np.concatenate([
+        rng.standard_normal(200000) * 50,
+        rng.standard_normal(50000) * 0.01,                      # subnormal range
+        np.array([O.e4m3_value(c) for c in range(127)]),        # exact values
+        (np.array([O.e4m3_value(c) for c in range(126)]) + np.array([O.e4m3_value(c) for c in range(1, 127)])) / 2,  # ties
+    ]).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(v), ref)
+
+
+def test_quantize_groups_bound_and_amax():
+    rng = np.random.default_rng(6)
+    v = (rng.standard_normal((32, 512)) * rng.uniform(0.01, 100, size=(32, 1))).astype(np.float32)
+    v[3, :128] = 0.0
+    q, s = O.quantize_groups(v)
+    deq = O.dequantize_groups(q, s)
+    assert s[3, 0] == 1.0 and np.all(q[3, :128] == 0)
+    # e4m3 keeps 3 mantissa bits: half-ulp relative bound 2^-4 for normals,
+    # absolute bound scale * 2^-10 in the subnormal range
+    bound = np.maximum(np.abs(v) * 2.0 ** -4, np.repeat(s, 128, axis=1) * 2.0 ** -10)
+    assert np.all(np.abs(deq - v) <= bound * (1 + 1e-6))
+    g = np.abs(v.reshape(32, 4, 128)).max(axis=2)
+    assert np.all((g == 0) | (np.abs(q.reshape(32, 4, 128)) .max(axis=2) > 0))
+    assert np.all(np.isin((q.reshape(32, 4, 128) & 0x7F).max(axis=2)[g > 0], [0x7E]))
+
+
+def test_quantize_blocks_matches_groups_on_blocks():
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((256, 384)).astype(np.float32)
+    q, s = O.quantize_blocks(w)
+    assert s.shape == (2, 3)
+    for bi in range(2):
+        for bj in range(3):
+            blk = w[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            assert s[bi, bj] == np.float32(np.abs(blk).max()) / np.float32(448)
+            ref = torch.from_numpy(blk / s[bi, bj]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(q[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128], ref)
+
+
+# ------------------------------------------------------------------ FFN and combine
+def torch_swiglu(x, wg, wu, wd):
+    x, wg, wu, wd = (torch.from_numpy(np.asarray(a, dtype=np.float64)) for a in (x, wg, wu, wd))
+    return (torch.nn.functional.silu(x @ wg) * (x @ wu)) @ wd
+
+
+def tiny_weights(cfg, seed):
+    rng = np.random.default_rng(seed)
+    W = {}
+    for e in range(cfg.E):
+        W[("w_gate", e)] = (rng.standard_normal((cfg.d, cfg.I)) / np.sqrt(cfg.d)).astype(np.float32)
+        W[("w_up", e)] = (rng.standard_normal((cfg.d, cfg.I)) / np.sqrt(cfg.d)).astype(np.float32)
+        W[("w_down", e)] = (rng.standard_normal((cfg.I, cfg.d)) / np.sqrt(cfg.I)).astype(np.float32)
+    for n in ("gate", "up", "down"):
+        W[("ws_" + n, 0)] = W[("w_" + n, 0)] * np.float32(0.5)
+    return lambda which, e: W[(which, e)]
+
+
+def test_ffn_single_expert_is_dense_swiglu():
+    cfg = mi.config(0).scaled(E=1, k=1, R=1)
+    x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    wt = tiny_weights(cfg, 9)
+    res = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)
+    ref = torch_swiglu(x, wt("w_gate", 0), wt("w_up", 0), wt("w_down", 0)).numpy()
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ffn_top1_uses_argmax_expert():
+    cfg = mi.config(0).scaled(k=1)
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
+    wt = tiny_weights(cfg, 11)
+    res = O.layer_forward(cfg, l, x, wt)
+    am = torch.argmax(torch.from_numpy(l), dim=1).numpy()
+    for t in range(cfg.T):
+        e = am[t]
+        ref = torch_swiglu(x[t:t + 1], wt("w_gate", e), wt("w_up", e), wt("w_down", e)).numpy()[0]
+        np.testing.assert_allclose(res["out"][t], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ffn_all_experts_softmax_mixture_with_shared():
+    cfg = mi.config(0).scaled(k=8, shared=True, T=8)
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
+    wt = tiny_weights(cfg, 13)
+    res = O.layer_forward(cfg, l, x, wt)
+    p = torch.softmax(torch.from_numpy(l).double(), dim=1)
+    ref = torch_swiglu(x, wt("ws_gate", 0), wt("ws_up", 0), wt("ws_down", 0))
+    for e in range(cfg.E):
+        ref = ref + p[:, e:e + 1] * torch_swiglu(x, wt("w_gate", e), wt("w_up", e), wt("w_down", e))
+    np.testing.assert_allclose(res["out"], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_identity_experts_return_x():
+    cfg = mi.config(0)
+    x = mi.make_x(cfg).astype(np.float64)
+    ids, w = O.route(mi.make_logits(cfg), cfg.k)
+    lay = O.dispatch_layout(ids, cfg.E, cfg.R)
+    xp = O.permute(x, lay["row_to_token"])
+    np.testing.assert_allclose(O.combine(xp, lay["slot_to_row"], w), x, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(O.combine(xp, lay["slot_to_row"], w, shared=x), 2 * x, rtol=1e-14, atol=1e-14)
+
+
+def test_dispatch_bytes_and_expert_size_arithmetic():
+    g = load("expert_arithmetic.json")
+    cfg = mi.config(1)
+    assert 3 * cfg.d * cfg.I == g["expert_params_glm"]
+    assert round(3 * cfg.d * cfg.I / 1e6, 1) == g["expert_mb_fp8_glm"]   # one byte per e4m3 weight
+    T = 4
+    x = np.zeros((T, cfg.d), dtype=np.uint16)                           # bf16 rows
+    ids = np.stack([np.arange(cfg.k)] * T).astype(np.int32)
+    lay = O.dispatch_layout(ids, cfg.E, cfg.R)
+    assert O.permute(x, lay["row_to_token"]).nbytes // T == g["a2a_bytes_per_token_glm"]
+    assert round(3 * 7168 * 2048 / 1e6) == g["expert_params_dsv3_approx_m"]
+    assert round(8 * 7168 * 1 / 1000) == g["dispatch_fp8_bytes_dsv3_approx_kb"]
+    assert round(8 * 7168 * 2 / 1000) == g["combine_bf16_bytes_dsv3_approx_kb"]
+
+
+# ------------------------------------------------------------------ planted mistakes
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Plant plausible slips in the oracle and check that a pin above fails."""
+    cfg = mi.config(0).scaled(E=1, k=1, R=1)
+    x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    wt = tiny_weights(cfg, 9)
+    ref = torch_swiglu(x, wt("w_gate", 0), wt("w_up", 0), wt("w_down", 0)).numpy()
+    real = O.swiglu_expert
+
+    def swapped(x64, wg, wu, wd, mode):           # gate and up exchanged
+        return real(x64, wu, wg, wd, mode)
+
+    monkeypatch.setattr(O, "swiglu_expert", swapped)
+    out = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)["out"]
+    assert not np.allclose(out, ref, rtol=1e-6, atol=1e-6)
+    monkeypatch.setattr(O, "swiglu_expert", real)
+
+    monkeypatch.setattr(O, "silu", lambda z: z / (1.0 + np.exp(z)))   # sign slip
+    out = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)["out"]
+    assert not np.allclose(out, ref, rtol=1e-6, atol=1e-6)
+    monkeypatch.undo()
+
+    # a tie-break slip (equal logits -> higher index) disagrees with the brute force
+    l = np.array([[1.0, 2.0, 2.0, 0.0]], dtype=np.float32)
+    ids_bad = 3 - np.argsort(-l[:, ::-1], axis=1, kind="stable")[:, :1]
+    assert set(ids_bad[0].tolist()) != brute_topk(l[0].tolist(), 1)
+    assert set(O.route(l, 1)[0][0].tolist()) == brute_topk(l[0].tolist(), 1)
+
+    # dropping the renormalisation (raw softmax probabilities) breaks sum(w) = 1
+    l = np.random.default_rng(1).standard_normal((4, 8)).astype(np.float32)
+    p = torch.softmax(torch.from_numpy(l).double(), 1).numpy()
+    ids, w = O.route(l, 2)
+    raw = np.take_along_axis(p, ids.astype(np.int64), 1)
+    assert not np.allclose(raw.sum(1), 1.0) and np.allclose(w.sum(1), 1.0)
