@@ -1,0 +1,39 @@
+// Internal interface of the expert-FFN implementations.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct FfnArgs {
+  const void *x_perm;      // [N, d] in the expert input dtype
+  const float *x_scales;   // e4m3: [N, d/128]
+  const int32_t *offs;     // [P + 1] physical expert offsets
+  const int32_t *p2l;      // [P] or null (identity)
+  int64_t P, N;
+  const moe_weights_t *w;
+  const void *shared_x;    // [T_shared, d] or null
+  int64_t T_shared;
+  void *h;                 // [N + T_shared, I] workspace (+ e4m3 scales after it)
+  float *h_scales;         // e4m3: [N + T_shared, I/128]
+  void *tiles;             // scheduling workspace
+  void *y;                 // [N + T_shared, d]
+  int32_t *err;
+};
+
+// Largest p in [0, P) with offs[p] <= row (callers guarantee row < offs[P]).
+__device__ __forceinline__ int group_of_row(const int32_t *offs, int P, int row) {
+  int lo = 0, hi = P - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offs[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+moe_status_t ffn_f32(const FfnArgs &a, cudaStream_t st);
+moe_status_t ffn_bf16(const FfnArgs &a, cudaStream_t st);
+moe_status_t ffn_e4m3(const FfnArgs &a, cudaStream_t st);
+
+}  // namespace moe

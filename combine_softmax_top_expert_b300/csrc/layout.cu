@@ -1,0 +1,344 @@
+// Dispatch layout and EPLB map.
+//
+// Layout ("6.4 Data parallelism and expert parallelism", section 3.1 step 2 and
+// its figure; section 5.1 busiest card / average): a stable, atomic-free counting
+// sort of the N = T*k slots by physical expert, in three launches.
+//
+//   count   one CTA per chunk of 2048 consecutive slots (slot s = t*k + j); each
+//           warp takes 256 slots in batches of 32.  __match_any_sync groups the
+//           lanes of a batch that share an expert; a lane's rank is the number of
+//           lower lanes in its group plus the warp's running count, so ranks follow
+//           slot order.  Slots of one expert come from distinct tokens, so slot
+//           order is token order.  A scan over the 8 warps turns warp ranks into
+//           chunk ranks; the chunk histogram goes to hist[chunk][P].
+//   scan    one CTA: column scans of hist give each chunk's base per expert and
+//           the expert counts; a block scan gives the expert offsets; rank counts,
+//           rank offsets and the load statistics follow.
+//   scatter row = offset[p] + chunk base[p] + chunk rank; slot_to_row, row_to_token.
+//
+// EPLB map ("6.4 ...", section 5.3; "How Expert Parallelism Works for
+// Mixture-of-Experts Models in vLLM", "MoE Layer Construction"): one CTA ranks the
+// experts by (count desc, index asc) and writes the physical tables.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 2048;        // slots per CTA in the count pass
+constexpr int kCountWarps = 8;      // 8 warps x 256 slots
+constexpr int kSlotsPerWarp = kChunk / kCountWarps;
+constexpr int kMaxP = 2048;
+
+struct PhysMap {
+  int E;
+  int k;
+  const int32_t *replica_count;    // null: identity map
+  const int32_t *logical_to_phys;  // [E, 2]
+};
+
+__device__ __forceinline__ int phys_of(const int32_t *ids, int64_t s, const PhysMap &m, int32_t *err) {
+  const int e = ids[s];
+  if (e < 0 || e >= m.E) {
+    raise_dev(err, MOE_DEV_ID_RANGE);
+    return -1;
+  }
+  if (!m.replica_count) return e;
+  const int64_t t = s / m.k;
+  const int rc = m.replica_count[e];
+  return m.logical_to_phys[2 * e + (int)(t % rc)];
+}
+
+__global__ void __launch_bounds__(256) layout_count_kernel(const int32_t *__restrict__ ids, int64_t N, int P,
+                                                           PhysMap m, int32_t *__restrict__ hist,
+                                                           int32_t *__restrict__ chunk_rank, int32_t *err) {
+  extern __shared__ int32_t cnt[];  // [kCountWarps][P]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kCountWarps * P; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kChunk + warp * kSlotsPerWarp;
+  int32_t *wc = cnt + warp * P;
+  int rank[kSlotsPerWarp / 32];
+  int phys[kSlotsPerWarp / 32];
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int b = 0; b < kSlotsPerWarp / 32; ++b) {
+    const int64_t s = base + b * 32 + lane;
+    const int p = s < N ? phys_of(ids, s, m, err) : -1;
+    const unsigned peers = __match_any_sync(kFull, p);
+    int r = -1;
+    if (p >= 0) r = wc[p] + __popc(peers & lt);
+    __syncwarp();
+    if (p >= 0 && lane == __ffs(peers) - 1) wc[p] += __popc(peers);
+    __syncwarp();
+    rank[b] = r;
+    phys[b] = p;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kCountWarps; ++w) {
+      const int v = cnt[w * P + p];
+      cnt[w * P + p] = run;
+      run += v;
+    }
+    hist[(int64_t)blockIdx.x * P + p] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < kSlotsPerWarp / 32; ++b) {
+    const int64_t s = base + b * 32 + lane;
+    if (s < N) chunk_rank[s] = phys[b] >= 0 ? wc[phys[b]] + rank[b] : -1;
+  }
+}
+
+struct StatsOut {
+  moe_load_stats_t *stats;  // [2]
+};
+
+// Warp-level statistics of `counts` [n] grouped into R ranks of n/R entries.
+__device__ void warp_stats(const int32_t *counts, int n, int R, int64_t total, moe_load_stats_t *out) {
+  const int lane = threadIdx.x & 31;
+  const int per = n / R;
+  int max_rank = 0, max_exp = 0, active = 0;
+  for (int r = lane; r < R; r += 32) {
+    int s = 0;
+    for (int i = 0; i < per; ++i) s += counts[r * per + i];
+    max_rank = max(max_rank, s);
+  }
+  for (int i = lane; i < n; i += 32) {
+    max_exp = max(max_exp, counts[i]);
+    active += counts[i] > 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    max_rank = max(max_rank, __shfl_xor_sync(kFull, max_rank, o));
+    max_exp = max(max_exp, __shfl_xor_sync(kFull, max_exp, o));
+    active += __shfl_xor_sync(kFull, active, o);
+  }
+  if (lane == 0) {
+    moe_load_stats_t st;
+    st.max_rank = max_rank;
+    st.max_expert = max_exp;
+    st.n_active_experts = active;
+    st.pad_ = 0;
+    st.mean_rank = (float)((double)total / (double)R);
+    st.max_over_mean = st.mean_rank > 0.f ? (float)((double)max_rank * R / (double)total) : 0.f;
+    st.balancedness = max_rank > 0 ? (float)((double)total / ((double)R * max_rank)) : 0.f;
+    st.pad2_ = 0.f;
+    *out = st;
+  }
+}
+
+__global__ void __launch_bounds__(1024) layout_scan_kernel(int32_t *__restrict__ hist, int chunks, int P, int E,
+                                                           int R, int64_t N, const int32_t *p2l,
+                                                           int32_t *logical_counts, int32_t *phys_counts,
+                                                           int32_t *phys_offsets, int32_t *rank_counts,
+                                                           int32_t *rank_offsets, moe_load_stats_t *stats) {
+  __shared__ int32_t cnt[kMaxP];
+  __shared__ int32_t lcnt[1024];
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t rcnt[kMaxP];
+  const int tid = threadIdx.x;
+  for (int p = tid; p < P; p += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < chunks; ++c) {
+      const int v = hist[(int64_t)c * P + p];
+      hist[(int64_t)c * P + p] = run;
+      run += v;
+    }
+    cnt[p] = run;
+    phys_counts[p] = run;
+  }
+  for (int e = tid; e < E; e += blockDim.x) lcnt[e] = 0;
+  __syncthreads();
+  // logical counts: physical counts folded through phys_to_logical (integer adds)
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int e = p2l ? p2l[p] : p;
+    if (e >= 0 && e < E) atomicAdd(&lcnt[e], cnt[p]);
+  }
+  // exclusive scan of cnt[0..P) -> offsets; each thread owns two consecutive entries
+  const int a = 2 * tid < P ? cnt[2 * tid] : 0;
+  const int b = 2 * tid + 1 < P ? cnt[2 * tid + 1] : 0;
+  int v = a + b;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, ws, o);
+      if (lane >= o) ws += n;
+    }
+    warp_sums[lane] = ws;
+  }
+  __syncthreads();
+  const int excl = v - (a + b) + (warp > 0 ? warp_sums[warp - 1] : 0);
+  if (2 * tid < P) phys_offsets[2 * tid] = excl;
+  if (2 * tid + 1 < P) phys_offsets[2 * tid + 1] = excl + a;
+  if (tid == 0) phys_offsets[P] = warp_sums[31];
+  // rank counts / offsets (linear placement, P/R physical experts per rank)
+  const int per = P / R;
+  for (int r = tid; r < R; r += blockDim.x) {
+    int s = 0;
+    for (int i = 0; i < per; ++i) s += cnt[r * per + i];
+    rcnt[r] = s;
+    rank_counts[r] = s;
+  }
+  for (int e = tid; e < E; e += blockDim.x) logical_counts[e] = lcnt[e];
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      int x = r < R ? rcnt[r] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += n;
+      }
+      if (r < R) rank_offsets[r] = run + x - rcnt[r];
+      run += __shfl_sync(kFull, x, 31);
+    }
+    if (lane == 0) rank_offsets[R] = run;
+  }
+  if (stats) {
+    if (warp == 1) warp_stats(lcnt, E, R, N, &stats[0]);
+    if (warp == 2) warp_stats(cnt, P, R, N, &stats[1]);
+  }
+}
+
+__global__ void __launch_bounds__(256) layout_scatter_kernel(const int32_t *__restrict__ ids, int64_t N, int P,
+                                                             PhysMap m, const int32_t *__restrict__ hist,
+                                                             const int32_t *__restrict__ chunk_rank,
+                                                             const int32_t *__restrict__ phys_offsets,
+                                                             int32_t *__restrict__ row_to_token,
+                                                             int32_t *__restrict__ slot_to_row) {
+  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= N) return;
+  const int r = chunk_rank[s];
+  if (r < 0) {
+    slot_to_row[s] = -1;
+    return;
+  }
+  const int p = phys_of(ids, s, m, nullptr);
+  const int row = phys_offsets[p] + hist[(s / kChunk) * P + p] + r;
+  slot_to_row[s] = row;
+  row_to_token[row] = (int32_t)(s / m.k);
+}
+
+__global__ void __launch_bounds__(1024) eplb_map_kernel(const int32_t *__restrict__ counts, int E, int R, int n_red,
+                                                        int32_t *phys_to_logical, int32_t *phys_rank,
+                                                        int32_t *replica_count, int32_t *logical_to_phys) {
+  __shared__ int32_t c[1024];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = counts[e];
+  __syncthreads();
+  const int base = E / R, S = (E + n_red) / R;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int ce = c[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) rank += (c[f] > ce) || (c[f] == ce && f < e);
+    const int pr = (e / base) * S + e % base;
+    phys_to_logical[pr] = e;
+    phys_rank[pr] = e / base;
+    logical_to_phys[2 * e] = pr;
+    if (rank < n_red) {
+      const int r = rank % R, slot = base + rank / R;
+      const int pp = r * S + slot;
+      phys_to_logical[pp] = e;
+      phys_rank[pp] = r;
+      logical_to_phys[2 * e + 1] = pp;
+      replica_count[e] = 2;
+    } else {
+      logical_to_phys[2 * e + 1] = -1;
+      replica_count[e] = 1;
+    }
+  }
+}
+
+}  // namespace
+
+size_t dispatch_ws_bytes(int64_t T, int32_t k, int64_t P) {
+  const int64_t N = T * k;
+  const int64_t chunks = (N + kChunk - 1) / kChunk;
+  return align_up((size_t)(chunks * P) * 4, 256) + align_up((size_t)N * 4, 256);
+}
+
+moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int64_t E, int32_t R,
+                             const moe_eplb_t *eplb, int32_t *logical_counts, int32_t *phys_counts,
+                             int32_t *phys_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                             int32_t *row_to_token, int32_t *slot_to_row, moe_load_stats_t *stats, void *ws,
+                             size_t ws_bytes, int32_t *err, cudaStream_t st) {
+  const int64_t P = eplb ? eplb->P : E;
+  if (T < 0 || k < 1 || E < 1 || E > 1024 || R < 1 || P < E || P > kMaxP || P % R || E % R)
+    return MOE_ERR_INVALID_ARG;
+  if (!logical_counts || !phys_counts || !phys_offsets || !rank_counts || !rank_offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (eplb && (!eplb->phys_to_logical || !eplb->replica_count || !eplb->logical_to_phys))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t N = T * k;
+  if (N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (N > 0 && (!topk_ids || !row_to_token || !slot_to_row)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < dispatch_ws_bytes(T, k, P) || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  const int chunks = (int)((N + kChunk - 1) / kChunk);
+  int32_t *hist = static_cast<int32_t *>(ws);
+  int32_t *chunk_rank = reinterpret_cast<int32_t *>(static_cast<char *>(ws) +
+                                                    align_up((size_t)chunks * P * 4, 256));
+  PhysMap m{(int)E, k, eplb ? eplb->replica_count : nullptr, eplb ? eplb->logical_to_phys : nullptr};
+  if (chunks > 0) {
+    const size_t smem = (size_t)kCountWarps * P * 4;
+    if (smem > 48 * 1024) {
+      if (cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    layout_count_kernel<<<chunks, 256, smem, st>>>(topk_ids, N, (int)P, m, hist, chunk_rank, err);
+  }
+  layout_scan_kernel<<<1, 1024, 0, st>>>(hist, chunks, (int)P, (int)E, R, N,
+                                         eplb ? eplb->phys_to_logical : nullptr, logical_counts, phys_counts,
+                                         phys_offsets, rank_counts, rank_offsets, stats);
+  if (N > 0)
+    layout_scatter_kernel<<<(unsigned)((N + 255) / 256), 256, 0, st>>>(topk_ids, N, (int)P, m, hist, chunk_rank,
+                                                                       phys_offsets, row_to_token, slot_to_row);
+  return launch_status();
+}
+
+moe_status_t eplb_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_red, int32_t *phys_to_logical,
+                      int32_t *phys_rank, int32_t *replica_count, int32_t *logical_to_phys, cudaStream_t st) {
+  if (E < 1 || E > 1024 || R < 1 || E % R || n_red < 0 || n_red % R || n_red > E) return MOE_ERR_INVALID_ARG;
+  if (!logical_counts || !phys_to_logical || !phys_rank || !replica_count || !logical_to_phys)
+    return MOE_ERR_INVALID_ARG;
+  eplb_map_kernel<<<1, 1024, 0, st>>>(logical_counts, (int)E, R, n_red, phys_to_logical, phys_rank, replica_count,
+                                      logical_to_phys);
+  return launch_status();
+}
+
+}  // namespace moe
+
+MOE_API size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P) {
+  if (T < 0 || k < 1 || P < 1) return 0;
+  return moe::dispatch_ws_bytes(T, k, P);
+}
+
+MOE_API moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int64_t E, int32_t R,
+                                         const moe_eplb_t *eplb, int32_t *logical_counts, int32_t *phys_counts,
+                                         int32_t *phys_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                                         int32_t *row_to_token, int32_t *slot_to_row, moe_load_stats_t *stats,
+                                         void *ws, size_t ws_bytes, int32_t *err, moe_stream_t stream) {
+  return moe::dispatch_layout(topk_ids, T, k, E, R, eplb, logical_counts, phys_counts, phys_offsets, rank_counts,
+                              rank_offsets, row_to_token, slot_to_row, stats, ws, ws_bytes, err,
+                              moe::as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_redundant,
+                                  int32_t *phys_to_logical, int32_t *phys_rank, int32_t *replica_count,
+                                  int32_t *logical_to_phys, moe_stream_t stream) {
+  return moe::eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
+                       logical_to_phys, moe::as_cuda(stream));
+}

@@ -1,0 +1,264 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) routed mixture-of-experts layer forward.
+ *
+ * The layer, as "6.4 Data parallelism and expert parallelism" (section 3.1,
+ * "Dataflow inside one MoE layer") describes it, run on one GPU:
+ *
+ *   route    -> softmax over E experts, top-k experts and weights per token
+ *   dispatch -> count tokens per expert, scan, lay the k copies of every token out
+ *               expert-contiguously in expert-parallel rank order (the buffer an
+ *               all-to-all dispatch would send), per-rank load statistics
+ *   experts  -> grouped SwiGLU FFN (gate, up, down) per expert
+ *   combine  -> weighted sum of each token's k expert outputs (+ shared expert)
+ *
+ * Notation: T tokens, d hidden size, E routed (logical) experts, k experts per
+ * token, I expert intermediate size, R logical expert-parallel ranks,
+ * P = E + n_redundant physical experts, N = T*k routed rows.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; they must stay
+ *     valid until the work queued on `stream` has finished.  The library never
+ *     allocates, frees or keeps device memory between calls.  Struct arguments
+ *     (moe_shape_t, moe_weights_t, moe_eplb_t, moe_layer_aux_t) are HOST structs
+ *     read during the call; the pointers inside them are device pointers.
+ *   - Tensors are dense and row-major.  bf16 is stored as uint16 bit patterns,
+ *     e4m3 as one byte (OCP FP8 E4M3, "fn": no infinities, max 448).
+ *   - Work is queued on `stream` and the call returns at once.  The returned
+ *     status reports host-side validation and launch errors only.
+ *   - Problems found on the device (a non-finite logit, an expert id out of
+ *     range, a pipeline wait that ran out) are OR-ed as MOE_DEV_* bits into the
+ *     caller's device word `err` (int32, may be NULL to ignore them); the caller
+ *     reads it after synchronising.  Kernels never trap.
+ *   - The library holds no global state; calls on different streams may run
+ *     concurrently when they share no output buffer.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned tensor          */
+  MOE_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement  */
+  MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than *_workspace_size */
+  MOE_ERR_CUDA = 4         /* a CUDA runtime/driver call failed (launch, attrs)  */
+} moe_status_t;
+
+/* Bits OR-ed into the caller's device error word. */
+enum {
+  MOE_DEV_NONFINITE_LOGIT = 1, /* a router logit was NaN or +-Inf: ids/weights undefined */
+  MOE_DEV_ID_RANGE = 2,        /* an expert id outside [0, E): the slot was skipped      */
+  MOE_DEV_TIMEOUT = 4,         /* a pipeline wait gave up: outputs of that launch undefined */
+  MOE_DEV_LAYOUT = 8           /* expert offsets inconsistent with the rows: tile skipped */
+};
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype_t;
+
+/* Per-rank load statistics ("Your expert-parallel deployment is slower than the
+ * tensor-parallel one", "The three causes": max rank load against mean rank
+ * load; "6.4 ...", section 5.3: balancedness = average / max).  Loads count
+ * token-copies (t, j).  Written on the device. */
+typedef struct {
+  int32_t max_rank;         /* busiest rank's load                         */
+  int32_t max_expert;       /* busiest (physical or logical) expert's load */
+  int32_t n_active_experts; /* experts with at least one row               */
+  int32_t pad_;
+  float mean_rank;          /* T*k / R                                     */
+  float max_over_mean;      /* max_rank / mean_rank                        */
+  float balancedness;       /* mean_rank / max_rank                        */
+  float pad2_;
+} moe_load_stats_t;
+
+/* EPLB replica map (device arrays), as written by moe_eplb_map. */
+typedef struct {
+  int32_t P;                      /* physical experts, E + n_redundant        */
+  const int32_t *phys_to_logical; /* [P]                                       */
+  const int32_t *replica_count;   /* [E], 1 or 2                               */
+  const int32_t *logical_to_phys; /* [E, 2]: primary, replica (-1 when none)   */
+} moe_eplb_t;
+
+/* Packed expert weights (produced by moe_pack_weights), one set per logical
+ * expert; with has_shared the set at index E is the always-on shared expert.
+ *   w13: [E_w, 2I, d]  rows 0..I-1 = W_gate^T, rows I..2I-1 = W_up^T (d contiguous)
+ *   w2 : [E_w, d, I]   W_down^T (I contiguous)
+ *   e4m3 only: s13 [E_w, 2I/128, d/128], s2 [E_w, d/128, I/128] fp32 block scales,
+ *   dequantised weight = code * scale of its 128x128 block. */
+typedef struct {
+  moe_dtype_t dtype; /* MOE_F32, MOE_BF16 or MOE_E4M3 */
+  int32_t has_shared;
+  int64_t E_w, d, I;
+  const void *w13;
+  const void *w2;
+  const float *s13;
+  const float *s2;
+} moe_weights_t;
+
+/* Whole-layer shape and precision. */
+typedef struct {
+  int64_t T, d, E, I;
+  int32_t k, R;
+  int32_t n_redundant;      /* EPLB replicas, 0 = off; must be a multiple of R and <= E */
+  int32_t shared;           /* 1 = always-on shared expert (weight set E, weight 1)     */
+  moe_dtype_t act_dtype;    /* x and out: MOE_F32 (with f32 experts) or MOE_BF16        */
+  moe_dtype_t expert_dtype; /* MOE_F32, MOE_BF16 or MOE_E4M3                            */
+} moe_shape_t;
+
+/* Optional device buffers that receive the layer's intermediate results; any
+ * NULL member is kept in the workspace instead. */
+typedef struct {
+  int32_t *topk_ids;        /* [T, k]   */
+  float *topk_w;            /* [T, k]   */
+  int32_t *logical_counts;  /* [E]      */
+  int32_t *phys_counts;     /* [P]      */
+  int32_t *phys_offsets;    /* [P + 1]  */
+  int32_t *rank_counts;     /* [R]      */
+  int32_t *rank_offsets;    /* [R + 1]  */
+  int32_t *row_to_token;    /* [N]      */
+  int32_t *slot_to_row;     /* [T, k]   */
+  moe_load_stats_t *stats;  /* [2]: before, after EPLB */
+  int32_t *phys_to_logical; /* [P]      */
+  int32_t *phys_rank;       /* [P]      */
+  int32_t *replica_count;   /* [E]      */
+  int32_t *logical_to_phys; /* [E, 2]   */
+} moe_layer_aux_t;
+
+/* Static text for a status code. */
+const char *moe_status_string(moe_status_t s);
+
+/* Route ("6.4 ...", section 3.1, step 1 "Route": top-k experts and weights per
+ * token).  logits [T, E] fp32.  Experts are chosen by (logit descending, index
+ * ascending); -0 and +0 tie.  topk_ids [T, k] int32 in that order; topk_w [T, k]
+ * fp32 = softmax over all E renormalised over the k chosen, i.e.
+ * exp(l_j - l_max) / sum over the chosen of exp(l_i - l_max).
+ * Limits: 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 queues nothing). */
+moe_status_t moe_route(const float *logits, int64_t T, int64_t E, int32_t k,
+                       int32_t *topk_ids, float *topk_w, int32_t *err,
+                       moe_stream_t stream);
+
+/* EPLB one-step replica map ("6.4 ...", section 5.3: (experts + redundant)/EP
+ * physical experts per card; "How Expert Parallelism Works for Mixture-of-Experts
+ * Models in vLLM", "MoE Layer Construction": num_physical = E + redundant).
+ * logical_counts [E] int32 (tokens per logical expert).  The n_redundant hottest
+ * experts (count descending, index ascending) get one replica each.  Rank r holds
+ * S = P/R physical slots: slots 0..E/R-1 are logical experts r*E/R + slot, then the
+ * replicas, the j-th hottest on rank j mod R in slot E/R + j/R; physical id =
+ * r*S + slot.  Outputs: phys_to_logical [P], phys_rank [P], replica_count [E],
+ * logical_to_phys [E, 2].  Requires E % R == 0, n_redundant % R == 0,
+ * 0 <= n_redundant <= E, E <= 1024. */
+moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int32_t R,
+                          int32_t n_redundant, int32_t *phys_to_logical,
+                          int32_t *phys_rank, int32_t *replica_count,
+                          int32_t *logical_to_phys, moe_stream_t stream);
+
+/* Bytes of workspace moe_dispatch_layout needs. */
+size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P);
+
+/* Dispatch layout ("6.4 ...", section 3.1, step 2 "Dispatch" and its figure:
+ * each token is copied k times to the cards that own its experts; section 5.1:
+ * busiest card / average).  topk_ids [T, k] int32 in [0, E).  Physical expert of
+ * slot (t, j): e, or with `eplb` logical_to_phys[e][t mod replica_count[e]].
+ * Physical experts are numbered rank-major (linear placement, P/R per rank), so
+ * rows sorted by physical expert are sorted by (rank, expert); inside an expert,
+ * rows are in ascending token order.  Outputs (device, int32):
+ *   logical_counts [E], phys_counts [P], phys_offsets [P+1] (exclusive scan),
+ *   rank_counts [R], rank_offsets [R+1], row_to_token [N], slot_to_row [T, k];
+ *   stats [2] (moe_load_stats_t): [0] logical experts over R ranks linearly
+ *   (before replication), [1] the physical layout (after; equal to [0] without EPLB).
+ * ws: moe_dispatch_workspace_size(T, k, P) bytes, 256-byte aligned.
+ * Ids out of range set MOE_DEV_ID_RANGE; those slots are left out of the layout.
+ * Limits: P <= 2048, P % R == 0, E % R == 0. */
+moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
+                                 int64_t E, int32_t R, const moe_eplb_t *eplb,
+                                 int32_t *logical_counts, int32_t *phys_counts,
+                                 int32_t *phys_offsets, int32_t *rank_counts,
+                                 int32_t *rank_offsets, int32_t *row_to_token,
+                                 int32_t *slot_to_row, moe_load_stats_t *stats,
+                                 void *ws, size_t ws_bytes, int32_t *err,
+                                 moe_stream_t stream);
+
+/* Dispatch copy ("6.4 ...", section 3.1, step 2: copy each token's hidden state k
+ * times; section 3.2: dispatch in FP8).  x [T, d] (MOE_F32 or MOE_BF16) ->
+ * x_perm [N, d] with x_perm[slot_to_row[t, j]] = x[t].  perm_dt equal to x_dt is a
+ * plain copy; perm_dt = MOE_E4M3 (from bf16) quantises each token per 128-channel
+ * group: scale = amax/448 in fp32 (1 when amax = 0), code = e4m3(v / scale) with
+ * round-to-nearest-even and saturation; perm_scales [N, d/128] fp32.
+ * Requires d % 8 == 0 (d % 128 == 0 for e4m3), 16-byte aligned x and x_perm. */
+moe_status_t moe_permute(const void *x, moe_dtype_t x_dt, int64_t T, int64_t d,
+                         int32_t k, const int32_t *slot_to_row, void *x_perm,
+                         moe_dtype_t perm_dt, float *perm_scales,
+                         moe_stream_t stream);
+
+/* Bytes of workspace moe_expert_ffn needs (the intermediate h and tile tables). */
+size_t moe_ffn_workspace_size(int64_t rows, int64_t I, moe_dtype_t expert_dtype);
+
+/* Grouped SwiGLU expert FFN ("6.4 ...", section 2.1: one expert is the three
+ * matrices gate, up, down; section 7: the shared expert is a must-pick expert).
+ * For physical expert p with logical expert e = phys_to_logical[p] (identity when
+ * NULL), rows phys_offsets[p] .. phys_offsets[p+1]-1 of x_perm:
+ *   h = silu(x W_gate[e]) * (x W_up[e]);  y = h W_down[e]
+ * y_perm [N (+T), d].  With w->has_shared and shared_x != NULL, the shared expert
+ * (weight set E) runs on shared_x [T_shared, d] and writes rows N .. N+T_shared-1.
+ * Precision: f32 weights -> fp32 FFMA throughout (y fp32).  bf16 -> tensor cores,
+ * fp32 accumulate, h stored as bf16, y bf16.  e4m3 -> x_perm e4m3 + x_scales
+ * [N, d/128]; tensor cores per 128-deep K block with fp32 promotion by the
+ * block scales; h quantised per row per 128 channels (same rule as moe_permute);
+ * y bf16.  `rows_hint` is the number of routed rows N (phys_offsets[P] on the
+ * device must equal it).  ws: moe_ffn_workspace_size(N + T_shared, I, dtype).
+ * Limits (tensor-core paths): d % 128 == 0, I % 128 == 0. */
+moe_status_t moe_expert_ffn(const void *x_perm, const float *x_scales,
+                            const int32_t *phys_offsets, int64_t P,
+                            const int32_t *phys_to_logical, int64_t rows_hint,
+                            const moe_weights_t *w, const void *shared_x,
+                            int64_t T_shared, void *y_perm, void *ws,
+                            size_t ws_bytes, int32_t *err, moe_stream_t stream);
+
+/* Combine ("6.4 ...", section 3.1, step 4: weighted-sum by route weights).
+ * out[t] = sum_{j<k} topk_w[t, j] * y_perm[slot_to_row[t, j]] (+ shared_y[t]),
+ * fp32 accumulation in j order, then rounded to out_dt.  y_perm [N, d] and shared_y
+ * [T, d] (nullable) in y_dt (MOE_F32 or MOE_BF16); out [T, d] in out_dt. */
+moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_dt,
+                         const int32_t *slot_to_row, const float *topk_w,
+                         int64_t T, int32_t k, int64_t d, const void *shared_y,
+                         void *out, moe_dtype_t out_dt, moe_stream_t stream);
+
+/* One-time weight packing for one expert (not part of the timed forward).
+ * Logical w_gate [d, I], w_up [d, I], w_down [I, d] in src_dt (MOE_F32 or
+ * MOE_BF16) -> w13_e [2I, d] and w2_e [d, I] in dst_dt (the transposes, see
+ * moe_weights_t).  dst_dt = MOE_E4M3 (from bf16 or f32) quantises per 128x128
+ * block of the logical matrices with the moe_permute rule and writes the block
+ * scales s13_e [2I/128, d/128] and s2_e [d/128, I/128]. */
+moe_status_t moe_pack_weights(const void *w_gate, const void *w_up,
+                              const void *w_down, moe_dtype_t src_dt, int64_t d,
+                              int64_t I, moe_dtype_t dst_dt, void *w13_e,
+                              void *w2_e, float *s13_e, float *s2_e,
+                              moe_stream_t stream);
+
+/* Bytes of workspace moe_layer_forward needs. */
+size_t moe_layer_workspace_size(const moe_shape_t *shape);
+
+/* The whole layer forward on one stream: route -> dispatch layout (-> EPLB map
+ * on this batch's counts and the physical layout) -> permute -> expert FFN
+ * (+ shared expert) -> combine.  logits [T, E] fp32, x [T, d] in act_dtype,
+ * out [T, d] in act_dtype.  `aux` (nullable, host struct) exposes intermediate
+ * results.  ws: moe_layer_workspace_size(shape) bytes, 256-byte aligned.  No host
+ * synchronisation happens inside. */
+moe_status_t moe_layer_forward(const moe_shape_t *shape, const float *logits,
+                               const void *x, const moe_weights_t *w, void *out,
+                               const moe_layer_aux_t *aux, void *ws,
+                               size_t ws_bytes, int32_t *err,
+                               moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads and exports every entry point of include/moe.h;
+host-side validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_softmax_top_expert_b300 as moe
+from combine_softmax_top_expert_b300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe.EXPORTED) == names
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(moe.LoadStats) == 32
+    assert ctypes.sizeof(moe.Weights) == 64
+    assert ctypes.sizeof(moe.Shape) == 56
+    assert ctypes.sizeof(moe.LayerAux) == 14 * 8
+
+
+def test_status_strings(lib):
+    assert moe.moe_status_string(0) == "ok"
+    assert "invalid" in moe.moe_status_string(1)
+    assert "workspace" in moe.moe_status_string(3)
+
+
+def test_host_validation_without_gpu(lib):
+    # invalid shapes are rejected on the host before any CUDA call
+    L = moe.lib()
+    assert L.moe_route(None, -1, 8, 2, None, None, None, None) == 1
+    assert L.moe_route(None, 4, 8, 9, None, None, None, None) == 1         # k > E
+    assert L.moe_route(None, 4, 2000, 2, None, None, None, None) == 1      # E > 1024
+    assert L.moe_route(None, 0, 8, 2, None, None, None, None) == 0         # empty batch: nothing queued
+    assert L.moe_eplb_map(None, 256, 32, 33, None, None, None, None, None) == 1  # n_red % R
+    assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0
+    assert L.moe_combine(None, 1, None, None, 4, 2, 100, None, None, 1, None) == 1   # d % 8
+    ws = L.moe_dispatch_workspace_size(64, 2, 8)
+    assert ws > 0 and ws % 256 == 0
+    # a too-small workspace is reported as such
+    fake = ctypes.c_void_p(256)
+    assert L.moe_dispatch_layout(fake, 64, 2, 8, 4, None, fake, fake, fake, fake, fake, fake, fake, None,
+                                 fake, 16, None, None) == 3
+
+
+def test_layer_workspace_sizes(lib):
+    import moe_inputs as mi
+    for cfg in mi.CONFIGS:
+        s = moe.Shape()
+        s.T, s.d, s.E, s.I, s.k, s.R = cfg.T, cfg.d, cfg.E, cfg.I, cfg.k, cfg.R
+        s.n_redundant, s.shared = cfg.n_redundant, int(cfg.shared)
+        s.act_dtype = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
+        s.expert_dtype = {"fp32": moe.MOE_F32, "bf16": moe.MOE_BF16, "fp8": moe.MOE_E4M3}[cfg.dtype]
+        n = moe.moe_layer_workspace_size(s)
+        rows = cfg.N + (cfg.T if cfg.shared else 0)
+        # at least x_perm + y_perm + h
+        elem = {"fp32": 4, "bf16": 2, "fp8": 1}[cfg.dtype]
+        assert n >= cfg.N * cfg.d * elem + rows * cfg.d * (4 if cfg.dtype == "fp32" else 2) + rows * cfg.I * elem
+    s = moe.Shape()
+    s.T, s.d, s.E, s.I, s.k, s.R, s.act_dtype, s.expert_dtype = 4, 128, 8, 64, 2, 4, moe.MOE_F32, moe.MOE_BF16
+    assert moe.moe_layer_workspace_size(s) == 0    # fp32 activations need fp32 experts

@@ -1,0 +1,94 @@
+"""moe_layer_forward end to end on the five workloads, through the C ABI, against
+the CPU oracle.  Small cases compare every output; full-size workloads compare
+every routing/layout integer and the outputs of a sample of tokens (the oracle
+recomputes those tokens' expert rows one by one)."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import combine_softmax_top_expert_b300 as moe
+import moe_inputs as mi
+from combine_softmax_top_expert_b300.layer import Layer, PackedWeights, dtype_code
+from oracle import moe_oracle as O
+
+from _util import BF16_TOL, F32_TOL, FP8_RMS, close, dev_f32, dev_x, fill_weights, host_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def device_generated_weights(cfg):
+    """weight(which, e): the generator's logical matrix, drawn on the device and
+    copied to the host (the library never touches these)."""
+    @functools.lru_cache(maxsize=None)
+    def weight(which, e):
+        t = mi.make_weight_device(cfg, which, int(e), "cuda")
+        return t.cpu().numpy() if cfg.dtype == "fp32" else host_bf16_bits(t)
+    return weight
+
+
+def run_layer(cfg):
+    act = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
+    ex = dtype_code(cfg.dtype)
+    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
+    fill_weights(cfg, pw)
+    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw)
+    logits = mi.make_logits(cfg)
+    x = mi.make_x(cfg)
+    out = layer.forward(dev_f32(logits), dev_x(cfg, x))
+    torch.cuda.synchronize()
+    assert int(layer.err.item()) == 0
+    return layer, logits, x, out.float().cpu().numpy()
+
+
+def check(cfg, sample=None):
+    layer, logits, x, out = run_layer(cfg)
+    b = {n: t.cpu().numpy() for n, t in layer.bufs.items()}
+    ref = O.layer_forward(cfg, logits, x, device_generated_weights(cfg), tokens=sample)
+    lay = ref["layout"]
+    assert np.array_equal(b["topk_ids"], ref["topk_ids"])
+    assert close(b["topk_w"], ref["topk_w"], F32_TOL)[0] == 0
+    assert np.array_equal(b["phys_counts"], lay["phys_counts"])
+    assert np.array_equal(b["phys_offsets"], lay["phys_offsets"])
+    assert np.array_equal(b["rank_counts"], lay["rank_counts"])
+    assert np.array_equal(b["row_to_token"], lay["row_to_token"])
+    assert np.array_equal(b["slot_to_row"], lay["slot_to_row"])
+    if cfg.n_redundant:
+        em = ref["eplb"]
+        assert np.array_equal(b["phys_to_logical"], em["phys_to_logical"])
+        assert np.array_equal(b["replica_count"], em["replica_count"])
+        assert np.array_equal(b["logical_to_phys"], em["logical_to_phys"])
+    st = layer.stats()
+    for s, r in zip(st, (lay["stats_before"], lay["stats_after"])):
+        assert s["max_rank"] == r["max_rank"]
+        assert s["max_over_mean"] == pytest.approx(r["max_over_mean"], rel=1e-6)
+    toks = ref["tokens"]
+    got = out[toks]
+    if cfg.dtype == "fp8":
+        rms = np.sqrt(np.mean((got - ref["out"]) ** 2))
+        assert rms <= FP8_RMS * np.sqrt(np.mean(ref["out"] ** 2)), rms
+    else:
+        nbad, mx = close(got, ref["out"], F32_TOL if cfg.dtype == "fp32" else BF16_TOL)
+        assert nbad == 0, (nbad, mx)
+    return layer, ref
+
+
+def test_layer_tiny_fp32_full():
+    check(mi.config(0))
+
+
+@pytest.mark.parametrize("T", [1, 3, 65])
+def test_layer_tiny_fp32_ragged(T):
+    check(mi.config(0).scaled(T=T))
+
+
+def test_device_generator_matches_host():
+    for ci in (1, 4):
+        cfg = mi.config(ci)
+        for which, e in (("w_gate", 0), ("w_down", 255)):
+            dev = host_bf16_bits(mi.make_weight_device(cfg, which, e, "cuda"))
+            assert np.array_equal(dev, mi.make_weight_host(cfg, which, e))
+    cfg = mi.config(2)
+    dev = host_bf16_bits(mi.make_weight_device(cfg, "ws_up", 0, "cuda"))
+    assert np.array_equal(dev, mi.make_weight_host(cfg, "ws_up", 0))

@@ -1,0 +1,278 @@
+"""GPU parity of each step of the layer against the CPU oracle, through the C ABI.
+Integer results (ids, counts, offsets, rows, replica map, e4m3 codes) must match
+bit for bit; floating-point results within the stated tolerances."""
+import numpy as np
+import pytest
+import torch
+
+import combine_softmax_top_expert_b300 as moe
+import moe_inputs as mi
+from combine_softmax_top_expert_b300.layer import PackedWeights
+from oracle import moe_oracle as O
+
+from _util import F32_TOL, BF16_TOL, close, dev_bf16, dev_f32, host_bf16_bits
+
+pytestmark = pytest.mark.gpu
+I32 = dict(dtype=torch.int32, device="cuda")
+
+
+# ------------------------------------------------------------------ route
+def gpu_route(logits, k, err=None):
+    T, E = logits.shape
+    L = dev_f32(logits)
+    ids = torch.full((T, k), -7, **I32)
+    w = torch.full((T, k), -7.0, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, **I32) if err is None else err
+    moe.moe_route(L, T, E, k, ids, w, err)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), int(err.item())
+
+
+def check_route(logits, k):
+    ids, w, err = gpu_route(logits, k)
+    rid, rw = O.route(logits, k)
+    assert err == 0
+    assert np.array_equal(ids, rid)
+    nbad, mx = close(w, rw, F32_TOL)
+    assert nbad == 0, mx
+
+
+@pytest.mark.parametrize("ci", range(5))
+def test_route_workloads(ci):
+    cfg = mi.config(ci)
+    check_route(mi.make_logits(cfg), cfg.k)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (3, 8, 2), (257, 33, 5), (100, 64, 32), (64, 1000, 8),
+                                   (513, 256, 8), (70, 1024, 32)])
+def test_route_shapes_and_ties(T, E, k):
+    rng = np.random.default_rng(T * 7 + E)
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    check_route(l, k)
+    # integer logits: heavy ties resolved to the lower index; signed zeros tie
+    li = rng.integers(-3, 4, size=(T, E)).astype(np.float32)
+    li[li == 0] = np.where(rng.random((li == 0).sum()) < 0.5, -0.0, 0.0)
+    check_route(li, k)
+
+
+def test_route_flags_non_finite():
+    l = np.zeros((8, 16), dtype=np.float32)
+    l[3, 5] = np.nan
+    l[6, 1] = np.inf
+    _, _, err = gpu_route(l, 2)
+    assert err & moe.MOE_DEV_NONFINITE_LOGIT
+
+
+# ------------------------------------------------------------------ layout / EPLB
+def gpu_layout(ids_np, E, R, eplb=None):
+    T, k = ids_np.shape
+    P = E if eplb is None else eplb["P"]
+    N = T * k
+    ids = torch.from_numpy(ids_np.astype(np.int32)).cuda()
+    out = {n: torch.full((m,), -9, **I32) for n, m in
+           (("lc", E), ("pc", P), ("po", P + 1), ("rc", R), ("ro", R + 1), ("r2t", max(N, 1)),
+            ("s2r", max(N, 1)))}
+    stats = torch.zeros(16, **I32)
+    wsb = moe.moe_dispatch_workspace_size(T, k, P)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, **I32)
+    ep = None
+    keep = []
+    if eplb is not None:
+        p2l = torch.from_numpy(eplb["phys_to_logical"]).cuda()
+        rc = torch.from_numpy(eplb["replica_count"]).cuda()
+        l2p = torch.from_numpy(eplb["logical_to_phys"]).cuda()
+        keep = [p2l, rc, l2p]
+        ep = moe.Eplb(P, p2l.data_ptr(), rc.data_ptr(), l2p.data_ptr())
+    moe.moe_dispatch_layout(ids, T, k, E, R, ep, out["lc"], out["pc"], out["po"], out["rc"], out["ro"], out["r2t"],
+                            out["s2r"], stats, ws, wsb, err)
+    torch.cuda.synchronize()
+    del keep
+    res = {n: t.cpu().numpy() for n, t in out.items()}
+    res["err"] = int(err.item())
+    raw = stats.cpu().numpy().tobytes()
+    res["stats"] = [moe.LoadStats.from_buffer_copy(raw[32 * i:32 * i + 32]) for i in range(2)]
+    return res
+
+
+def check_layout(ids, E, R, eplb=None):
+    T, k = ids.shape
+    N = T * k
+    g = gpu_layout(ids, E, R, eplb)
+    r = O.dispatch_layout(ids, E, R, eplb)
+    assert g["err"] == 0
+    assert np.array_equal(g["lc"], r["logical_counts"])
+    assert np.array_equal(g["pc"], r["phys_counts"])
+    assert np.array_equal(g["po"], r["phys_offsets"])
+    assert np.array_equal(g["rc"], r["rank_counts"])
+    assert np.array_equal(g["ro"], r["rank_offsets"])
+    assert np.array_equal(g["r2t"][:N], r["row_to_token"])
+    assert np.array_equal(g["s2r"][:N], r["slot_to_row"].ravel())
+    for gs, rs in zip(g["stats"], (r["stats_before"], r["stats_after"])):
+        assert gs.max_rank == rs["max_rank"]
+        assert gs.max_expert == rs["max_expert"]
+        assert gs.n_active_experts == rs["n_active_experts"]
+        assert gs.mean_rank == pytest.approx(rs["mean_rank"], rel=1e-6)
+        assert gs.max_over_mean == pytest.approx(rs["max_over_mean"], rel=1e-6)
+        assert gs.balancedness == pytest.approx(rs["balancedness"], rel=1e-6)
+    return g, r
+
+
+@pytest.mark.parametrize("ci", range(5))
+def test_layout_workloads(ci):
+    cfg = mi.config(ci)
+    ids, _ = O.route(mi.make_logits(cfg), cfg.k)
+    emap = None
+    if cfg.n_redundant:
+        emap = O.eplb_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.R, cfg.n_redundant)
+    check_layout(ids, cfg.E, cfg.R, emap)
+
+
+@pytest.mark.parametrize("T,E,k,R", [(1, 8, 2, 4), (3, 8, 2, 4), (257, 16, 4, 8), (2049, 256, 8, 64),
+                                     (5000, 64, 3, 2), (300, 1024, 32, 1)])
+def test_layout_shapes(T, E, k, R):
+    rng = np.random.default_rng(T + E + k)
+    ids, _ = O.route(rng.standard_normal((T, E)).astype(np.float32), k)
+    check_layout(ids, E, R)
+    # all tokens on one expert family: the most skewed histogram
+    ids2, _ = O.route(np.tile(np.arange(E, dtype=np.float32)[::-1], (T, 1)), k)
+    check_layout(ids2, E, R)
+
+
+@pytest.mark.parametrize("T,E,R,n_red", [(64, 8, 4, 4), (777, 64, 8, 16), (4096, 256, 32, 32)])
+def test_layout_with_eplb(T, E, R, n_red):
+    rng = np.random.default_rng(T)
+    l = rng.standard_normal((T, E)).astype(np.float32) + np.linspace(3, 0, E, dtype=np.float32)
+    ids, _ = O.route(l, 4)
+    emap = O.eplb_map(np.bincount(ids.ravel(), minlength=E), R, n_red)
+    check_layout(ids, E, R, emap)
+
+
+def test_layout_flags_out_of_range_ids():
+    ids = np.array([[0, 1], [2, 9], [-1, 3]], dtype=np.int32)
+    g = gpu_layout(ids, 8, 4)
+    assert g["err"] & moe.MOE_DEV_ID_RANGE
+    assert g["s2r"][3] == -1 and g["s2r"][4] == -1
+    assert g["pc"].sum() == 4 and g["po"][-1] == 4
+
+
+@pytest.mark.parametrize("E,R,n_red", [(8, 4, 4), (256, 32, 32), (256, 64, 64), (1024, 8, 8)])
+def test_eplb_map(E, R, n_red):
+    rng = np.random.default_rng(E + R)
+    counts = rng.integers(0, 20, size=E).astype(np.int32)      # many ties
+    ref = O.eplb_map(counts, R, n_red)
+    P = E + n_red
+    c = torch.from_numpy(counts).cuda()
+    p2l, prank = torch.full((P,), -9, **I32), torch.full((P,), -9, **I32)
+    rc, l2p = torch.full((E,), -9, **I32), torch.full((E, 2), -9, **I32)
+    moe.moe_eplb_map(c, E, R, n_red, p2l, prank, rc, l2p)
+    torch.cuda.synchronize()
+    assert np.array_equal(p2l.cpu().numpy(), ref["phys_to_logical"])
+    assert np.array_equal(prank.cpu().numpy(), ref["phys_rank"])
+    assert np.array_equal(rc.cpu().numpy(), ref["replica_count"])
+    assert np.array_equal(l2p.cpu().numpy(), ref["logical_to_phys"])
+
+
+# ------------------------------------------------------------------ permute / combine
+def layout_for(cfg):
+    ids, w = O.route(mi.make_logits(cfg), cfg.k)
+    return ids, w, O.dispatch_layout(ids, cfg.E, cfg.R)
+
+
+@pytest.mark.parametrize("ci,T", [(0, None), (1, None), (2, 1024), (4, 512)])
+def test_permute_copy_is_exact(ci, T):
+    cfg = mi.config(ci) if T is None else mi.config(ci).scaled(T=T)
+    ids, w, lay = layout_for(cfg)
+    x = mi.make_x(cfg)
+    dt = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
+    xd = dev_f32(x) if cfg.dtype == "fp32" else dev_bf16(x)
+    s2r = torch.from_numpy(lay["slot_to_row"].astype(np.int32)).cuda()
+    xp = torch.zeros((cfg.N, cfg.d), dtype=xd.dtype, device="cuda")
+    moe.moe_permute(xd, dt, cfg.T, cfg.d, cfg.k, s2r, xp, dt)
+    torch.cuda.synchronize()
+    ref = O.permute(x, lay["row_to_token"])
+    got = xp.cpu().numpy() if cfg.dtype == "fp32" else host_bf16_bits(xp)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("T,d", [(16384, 6144), (37, 128), (5, 384)])
+def test_permute_e4m3_codes_exact(T, d):
+    cfg = mi.config(4).scaled(T=T, d=d)
+    ids, w, lay = layout_for(cfg)
+    x = mi.make_x(cfg)
+    # add scale variety and exact zeros per group
+    xf = mi.f32_from_bf16_bits(x) * np.float32(7.5)
+    xf[1 % T, :128] = 0.0
+    x = mi.bf16_bits_from_f32(xf)
+    s2r = torch.from_numpy(lay["slot_to_row"].astype(np.int32)).cuda()
+    xq = torch.zeros((cfg.N, d), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((cfg.N, d // 128), dtype=torch.float32, device="cuda")
+    moe.moe_permute(dev_bf16(x), moe.MOE_BF16, T, d, cfg.k, s2r, xq, moe.MOE_E4M3, sc)
+    torch.cuda.synchronize()
+    q, s = O.quantize_groups(mi.f32_from_bf16_bits(x))
+    r2t = lay["row_to_token"]
+    assert np.array_equal(xq.cpu().numpy(), q[r2t])
+    assert np.array_equal(sc.cpu().numpy(), s[r2t])
+
+
+@pytest.mark.parametrize("ci,T", [(0, None), (1, None), (2, 2048)])
+def test_combine_and_identity_experts(ci, T):
+    cfg = mi.config(ci) if T is None else mi.config(ci).scaled(T=T)
+    ids, w, lay = layout_for(cfg)
+    rng = np.random.default_rng(ci)
+    y = rng.standard_normal((cfg.N, cfg.d)).astype(np.float32)
+    sh = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    dt = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
+    if dt == moe.MOE_BF16:
+        yb, shb = mi.bf16_bits_from_f32(y), mi.bf16_bits_from_f32(sh)
+        y, sh = mi.f32_from_bf16_bits(yb), mi.f32_from_bf16_bits(shb)
+        yd, shd = dev_bf16(yb), dev_bf16(shb)
+        tol = BF16_TOL
+    else:
+        yd, shd, tol = dev_f32(y), dev_f32(sh), F32_TOL
+    s2r = torch.from_numpy(lay["slot_to_row"].astype(np.int32)).cuda()
+    tw = dev_f32(w)
+    out = torch.empty((cfg.T, cfg.d), dtype=yd.dtype, device="cuda")
+    for shared in (None, shd):
+        moe.moe_combine(yd, dt, s2r, tw, cfg.T, cfg.k, cfg.d, shared, out, dt)
+        torch.cuda.synchronize()
+        ref = O.combine(y.astype(np.float64), lay["slot_to_row"], w, None if shared is None else sh)
+        got = out.float().cpu().numpy()
+        nbad, mx = close(got, ref, tol)
+        assert nbad == 0, mx
+    # identity experts: y = x_perm, weights renormalised -> out = x
+    x = mi.make_x(cfg)
+    xd = dev_f32(x) if dt == moe.MOE_F32 else dev_bf16(x)
+    xp = torch.empty((cfg.N, cfg.d), dtype=xd.dtype, device="cuda")
+    moe.moe_permute(xd, dt, cfg.T, cfg.d, cfg.k, s2r, xp, dt)
+    moe.moe_combine(xp, dt, s2r, tw, cfg.T, cfg.k, cfg.d, None, out, dt)
+    torch.cuda.synchronize()
+    xf = x if dt == moe.MOE_F32 else mi.f32_from_bf16_bits(x)
+    nbad, mx = close(out.float().cpu().numpy(), xf, (1e-6, 1e-6) if dt == moe.MOE_F32 else (0.0, 2 ** -8))
+    assert nbad == 0, mx
+
+
+# ------------------------------------------------------------------ weight packing
+@pytest.mark.parametrize("dst", ["bf16", "fp8", "fp32"])
+def test_pack_weights(dst):
+    d, I = 256, 384
+    cfg = mi.config(1).scaled(d=d, I=I, dtype="fp32" if dst == "fp32" else "bf16")
+    code = {"bf16": moe.MOE_BF16, "fp8": moe.MOE_E4M3, "fp32": moe.MOE_F32}[dst]
+    pw = PackedWeights(2, d, I, code, False)
+    wg, wu, wd = (mi.make_weight_host(cfg, n, 1) for n in ("w_gate", "w_up", "w_down"))
+    devw = [dev_f32(a) if dst == "fp32" else dev_bf16(a) for a in (wg, wu, wd)]
+    pw.pack(1, *devw)
+    torch.cuda.synchronize()
+    if dst == "fp32":
+        assert np.array_equal(pw.w13[1].cpu().numpy(), np.concatenate([wg.T, wu.T]))
+        assert np.array_equal(pw.w2[1].cpu().numpy(), wd.T)
+    elif dst == "bf16":
+        assert np.array_equal(host_bf16_bits(pw.w13[1]), np.concatenate([wg.T, wu.T]))
+        assert np.array_equal(host_bf16_bits(pw.w2[1]), wd.T)
+    else:
+        f = [mi.f32_from_bf16_bits(a) for a in (wg, wu, wd)]
+        qs = [O.quantize_blocks(a) for a in f]
+        assert np.array_equal(pw.w13[1].cpu().numpy(), np.concatenate([qs[0][0].T, qs[1][0].T]))
+        assert np.array_equal(pw.w2[1].cpu().numpy(), qs[2][0].T)
+        assert np.array_equal(pw.s13[1].cpu().numpy(), np.concatenate([qs[0][1].T, qs[1][1].T]))
+        assert np.array_equal(pw.s2[1].cpu().numpy(), qs[2][1].T)
