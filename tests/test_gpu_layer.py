@@ -92,3 +92,29 @@ def test_device_generator_matches_host():
     cfg = mi.config(2)
     dev = host_bf16_bits(mi.make_weight_device(cfg, "ws_up", 0, "cuda"))
     assert np.array_equal(dev, mi.make_weight_host(cfg, "ws_up", 0))
+
+
+# ------------------------------------------------------------------ bf16 workloads
+def sample_tokens(T, n=6, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1, T // 2], rng.integers(0, T, n)]))
+
+
+def test_layer_bf16_small_full():
+    check(mi.config(2).scaled(T=200, d=256, E=16, I=256, R=4))
+
+
+def test_layer_bf16_small_eplb_full():
+    check(mi.config(3).scaled(T=200, d=256, E=16, I=256, R=4, n_redundant=4))
+
+
+def test_layer_decode_bf16():
+    check(mi.config(1), sample=sample_tokens(128))
+
+
+def test_layer_prefill_bf16_skew():
+    check(mi.config(2), sample=sample_tokens(8192, n=3))
+
+
+def test_layer_prefill_bf16_skew_eplb():
+    check(mi.config(3), sample=sample_tokens(8192, n=3, seed=1))
