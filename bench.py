@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE layer forward on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (route -> dispatch layout -> permute ->
+gate/up GEMM + SwiGLU -> down GEMM -> combine) over one synthetic batch whose
+inputs are already in HBM.  Each of the six stages is a C-ABI call of
+libmoe_b300.so; CUDA events between them give each kernel's duration on the
+launching stream.  L2 is flushed (a 512 MiB write) between timed steps, outside
+the timed spans.  Under torchrun every rank runs its own batch on its own GPU
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (oracle/, plain float64 numpy) on the host
+cores instead, one token of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer tokens/s on 1 B300; grouped-GEMM % tensor peak; permute GB/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8, help="tokens in the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", action="append", default=[], metavar="FIELD=INT",
+                    help="change a shape field of the workload (T, E, R, k, d, I), e.g. for a small profiling case")
+    return ap.parse_args()
+
+
+def workload(args):
+    cfg = mi.config(args.workload)
+    if args.override:
+        kw = {}
+        for o in args.override:
+            key, val = o.split("=")
+            kw[key] = int(val)
+        cfg = cfg.scaled(name=cfg.name + "[" + ",".join(args.override) + "]", **kw)
+    return cfg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def workload_config(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "R": cfg.R,
+            "shared_expert": cfg.shared, "redundant_experts": cfg.n_redundant, "experts_dtype": cfg.dtype,
+            "l2": "flushed between timed steps (512 MiB write)", "parallelism": "independent batch per GPU"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if _has_cuda() else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _has_cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+def dist_max(v):
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        return v
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons while running."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.1)
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        self.out.seek(0)
+        rows = [r.split(", ") for r in self.out.read().strip().splitlines()]
+        rows = [r for r in rows if len(r) >= 9 and (not self.uuid or r[0].strip() == self.uuid)]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"{kernel}@{workload}")
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec.get("source_sha256") else None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import combine_softmax_top_expert_b300 as moe
+    from combine_softmax_top_expert_b300.layer import Layer, PackedWeights, dtype_code
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload(args)
+    act = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
+    ex = dtype_code(cfg.dtype)
+    T, E, k, R, d, I, P, N = cfg.T, cfg.E, cfg.k, cfg.R, cfg.d, cfg.I, cfg.P, cfg.N
+    T_sh = T if cfg.shared else 0
+    rows = N + T_sh
+
+    # weights: drawn on the device expert by expert, packed by the library
+    pw = PackedWeights(E, d, I, ex, cfg.shared, device=dev)
+    for e in range(E):
+        pw.pack(e, *(mi.make_weight_device(cfg, w, e, dev) for w in ("w_gate", "w_up", "w_down")))
+    if cfg.shared:
+        pw.pack(E, *(mi.make_weight_device(cfg, w, 0, dev) for w in ("ws_gate", "ws_up", "ws_down")))
+    W = pw.struct()
+    logits_np, x_np = mi.make_logits(cfg), mi.make_x(cfg)
+    logits = torch.from_numpy(logits_np).to(dev)
+    xt = torch.from_numpy(x_np if cfg.dtype == "fp32" else x_np.view(np.int16)).to(dev)
+    x = xt if cfg.dtype == "fp32" else xt.view(torch.bfloat16)
+
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids, tw = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    lc, pc, po = torch.empty(E, **i32), torch.empty(P, **i32), torch.empty(P + 1, **i32)
+    rc, ro = torch.empty(R, **i32), torch.empty(R + 1, **i32)
+    r2t, s2r = torch.empty(N, **i32), torch.empty((T, k), **i32)
+    stats = torch.empty(16, **i32)
+    p2l, prank, repc, l2p = torch.empty(P, **i32), torch.empty(P, **i32), torch.empty(E, **i32), torch.empty((E, 2), **i32)
+    dws_b = moe.moe_dispatch_workspace_size(T, k, P)
+    dws = torch.empty(dws_b, dtype=torch.uint8, device=dev)
+    elt = {moe.MOE_F32: torch.float32, moe.MOE_BF16: torch.bfloat16, moe.MOE_E4M3: torch.uint8}
+    xp = torch.empty((N, d), dtype=elt[ex], device=dev)
+    xs = torch.empty((N, d // 128), dtype=torch.float32, device=dev) if ex == moe.MOE_E4M3 else None
+    h = torch.empty((rows, I), dtype=elt[ex] if ex != moe.MOE_BF16 else torch.bfloat16, device=dev)
+    hs = torch.empty((rows, I // 128), dtype=torch.float32, device=dev) if ex == moe.MOE_E4M3 else None
+    y = torch.empty((rows, d), dtype=torch.float32 if act == moe.MOE_F32 else torch.bfloat16, device=dev)
+    out = torch.empty((T, d), dtype=y.dtype, device=dev)
+    err = torch.zeros(1, **i32)
+    eplb = moe.Eplb(P, p2l.data_ptr(), repc.data_ptr(), l2p.data_ptr()) if cfg.n_redundant else None
+    y_dt = moe.MOE_F32 if act == moe.MOE_F32 else moe.MOE_BF16
+    perm_dt = ex if ex == moe.MOE_E4M3 else act
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stage_names = ["route", "dispatch_layout", "permute", "expert_gate_up", "expert_down", "combine"]
+    launches = {"route": 1, "dispatch_layout": 3 * (2 if cfg.n_redundant else 1) + (1 if cfg.n_redundant else 0),
+                "permute": 1, "expert_gate_up": 1, "expert_down": 1, "combine": 1}
+
+    def step(ev):
+        ev[0].record(stream)
+        moe.moe_route(logits, T, E, k, ids, tw, err)
+        ev[1].record(stream)
+        if cfg.n_redundant:
+            moe.moe_dispatch_layout(ids, T, k, E, R, None, lc, pc, po, rc, ro, r2t, s2r, stats, dws, dws_b, err)
+            moe.moe_eplb_map(lc, E, R, cfg.n_redundant, p2l, prank, repc, l2p)
+        moe.moe_dispatch_layout(ids, T, k, E, R, eplb, lc, pc, po, rc, ro, r2t, s2r, stats, dws, dws_b, err)
+        ev[2].record(stream)
+        moe.moe_permute(x, act, T, d, k, s2r, xp, perm_dt, xs)
+        ev[3].record(stream)
+        moe.moe_expert_gate_up(xp, xs, po, P, p2l if cfg.n_redundant else None, N, W, x if cfg.shared else None,
+                               T_sh, h, hs, err)
+        ev[4].record(stream)
+        moe.moe_expert_down(h, hs, po, P, p2l if cfg.n_redundant else None, N, W, T_sh, y, err)
+        ev[5].record(stream)
+        moe.moe_combine(y, y_dt, s2r, tw, T, k, d, y[N:] if cfg.shared else None, out, act)
+        ev[6].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+
+    for _ in range(max(args.warmup, 3)):
+        step(new_events())
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    # load statistics and the active experts of this batch (deterministic inputs)
+    pc_h = pc.cpu().numpy()
+    raw = stats.cpu().numpy().tobytes()
+    st = [moe.LoadStats.from_buffer_copy(raw[32 * i:32 * i + 32]) for i in range(2)]
+    p2l_h = p2l.cpu().numpy() if cfg.n_redundant else np.arange(P)
+    active_logical = len(set(p2l_h[pc_h > 0].tolist())) + (1 if cfg.shared else 0)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else None
+    evs = [new_events() for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+    barrier()
+    per_stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)])
+    total_ms = float(per_stage.sum())
+    total_ms_max = dist_max(total_ms)
+    value = world * T * args.steps / (total_ms_max / 1e3)
+
+    # ---------------- roofline of the dominant kernel (the gate/up GEMM)
+    pk = peaks()
+    sw = {"fp32": 4, "bf16": 2, "fp8": 1}[cfg.dtype]
+    sx = 4 if cfg.dtype == "fp32" else (1 if cfg.dtype == "fp8" else 2)
+    stage_ms = per_stage.mean(axis=0)
+    gu_bytes = active_logical * 2 * d * I * sw + rows * d * sx + rows * I * sx
+    dn_bytes = active_logical * d * I * sw + rows * I * sx + rows * d * (4 if act == moe.MOE_F32 else 2)
+    gu_flops = 2.0 * rows * d * 2 * I
+    dn_flops = 2.0 * rows * I * d
+    xb = 4 if act == moe.MOE_F32 else 2
+    perm_bytes = T * d * xb + N * d * (1 if cfg.dtype == "fp8" else xb) + (N * d // 128 * 4 if cfg.dtype == "fp8" else 0)
+    comb_bytes = N * d * (4 if act == moe.MOE_F32 else 2) + T_sh * d * xb + T * d * xb + N * 8
+    route_bytes = T * E * 4 + N * 8
+    weight_bound = rows / max(active_logical, 1) < 64   # few rows per expert: weight reads dominate
+    kernels = {}
+    for name, ms, byts, flops in (("route", stage_ms[0], route_bytes, 0), ("permute", stage_ms[2], perm_bytes, 0),
+                                  ("expert_gate_up", stage_ms[3], gu_bytes, gu_flops),
+                                  ("expert_down", stage_ms[4], dn_bytes, dn_flops),
+                                  ("combine", stage_ms[5], comb_bytes, 0)):
+        rec = {"ms": round(float(ms), 5), "GB/s": round(byts / (ms * 1e6), 1)}
+        if flops:
+            rec["TFLOP/s"] = round(flops / (ms * 1e9), 1)
+        kernels[name] = rec
+    kernels["dispatch_layout"] = {"ms": round(float(stage_ms[1]), 5)}
+    gu_ms = float(stage_ms[3])
+    if weight_bound or cfg.dtype == "fp32":
+        ach = gu_bytes / (gu_ms * 1e6)
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4)}
+    else:
+        ach = gu_flops / (gu_ms * 1e9)
+        peak = pk["bf16_tflops"] * (2.0 if cfg.dtype == "fp8" else 1.0)
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4)}
+    roof.update({"kernel": "expert_gate_up (grouped GEMM + SwiGLU)", "traffic": traffic_for("expert_gate_up", cfg.name),
+                 "peak_source": pk["source"] + (" (bf16 burst x 2 nominal fp8 ratio)" if cfg.dtype == "fp8" else ""),
+                 "algorithmic": (f"{active_logical} active experts x 2*d*I*{sw} B weights + x rows + h rows"
+                                 if roof["bound"] == "hbm" else "2*rows*d*2I flops")})
+
+    # ---------------- end to end through moe_layer_forward, host buffers
+    layer = Layer(T, d, E, k, I, R, act, ex, cfg.shared, cfg.n_redundant, pw, keep_aux=False, device=dev)
+    h_logits = torch.from_numpy(logits_np).pin_memory()
+    h_x = (torch.from_numpy(x_np) if cfg.dtype == "fp32" else torch.from_numpy(x_np.view(np.int16))).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_logits, d_xraw = torch.empty_like(logits), torch.empty_like(xt)
+    d_x = d_xraw if cfg.dtype == "fp32" else d_xraw.view(torch.bfloat16)
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_xraw.copy_(h_x, non_blocking=True)
+        o = layer.forward(d_logits, d_x)
+        h_out.copy_(o, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        e2e_step()
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = dist_max(sum(a.elapsed_time(b) for a, b in e_ev))
+    if int(layer.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(layer.err.item())}")
+    e2e = {"value": round(world * T * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * h_x.element_size()),
+           "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "api": "moe_layer_forward"}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator)",
+            "config": workload_config(cfg), "roofline": roof, "kernels": kernels, "e2e": e2e,
+            "gpu_launches": int(sum(launches.values()) * args.steps),
+            "load": {"max_over_mean_before": round(st[0].max_over_mean, 4),
+                     "max_over_mean_after": round(st[1].max_over_mean, 4),
+                     "active_experts": int(st[1].n_active_experts), "max_expert_rows": int(st[1].max_expert)},
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, logits_np, x_np, args.cpu_tokens, dev)
+    return line
+
+
+# ------------------------------------------------------------------ the oracle, timed
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+class host_cores:
+    """Let the oracle's BLAS calls use every host core while it is timed (the
+    environment may pin BLAS to one thread); its elementwise numpy work stays
+    single-threaded."""
+
+    def __enter__(self):
+        self.ctx = None
+        try:
+            from threadpoolctl import threadpool_limits
+            self.ctx = threadpool_limits(limits=os.cpu_count() or 1, user_api="blas")
+        except Exception:
+            pass
+        return self
+
+    def __exit__(self, *a):
+        if self.ctx is not None:
+            self.ctx.restore_original_limits()
+
+
+def sample_weights(cfg, tokens, logits, dev):
+    """Host copies of the logical weights the sampled tokens touch (drawn by the
+    generator on the device when there is one, else on the host)."""
+    from oracle import moe_oracle as O
+    ids, _ = O.route(logits, cfg.k)
+    need = {(w, int(e)) for t in tokens for e in ids[t] for w in ("w_gate", "w_up", "w_down")}
+    if cfg.n_redundant:
+        need = {(w, e) for w in ("w_gate", "w_up", "w_down") for e in range(cfg.E)} if len(tokens) > 4 else need
+    if cfg.shared:
+        need |= {(w, 0) for w in ("ws_gate", "ws_up", "ws_down")}
+    store = {}
+    for which, e in sorted(need):
+        if dev is not None:
+            import torch
+            t = mi.make_weight_device(cfg, which, e, dev)
+            store[(which, e)] = t.cpu().numpy() if cfg.dtype == "fp32" else t.view(torch.int16).cpu().numpy().view(np.uint16)
+        else:
+            store[(which, e)] = mi.make_weight_host(cfg, which, e)
+    return lambda which, e: store[(which, int(e))]
+
+
+def cpu_baseline(cfg, logits, x, n_tokens, dev):
+    from oracle import moe_oracle as O
+    tokens = np.arange(min(n_tokens, cfg.T))
+    weight = sample_weights(cfg, tokens, logits, dev)
+    with host_cores():
+        cores = oracle_threads()
+        t0 = time.perf_counter()
+        O.layer_forward(cfg, logits, x, weight, tokens=tokens)
+        dt = time.perf_counter() - t0
+    return {"value": round(len(tokens) / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(tokens)} tokens of {cfg.name} (routing and layout of all {cfg.T} tokens, the expert "
+                      f"FFN and combine of the sample), {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    from oracle import moe_oracle as O
+    cfg = workload(args)
+    logits, x = mi.make_logits(cfg), mi.make_x(cfg)
+    dev = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            dev = torch.device("cuda", 0)
+    except Exception:
+        dev = None
+    pool = np.arange(min(4, cfg.T))          # steps cycle over these tokens
+    weight = sample_weights(cfg, pool, logits, dev)
+    with host_cores():
+        cores = oracle_threads()
+        for i in range(args.warmup):
+            O.layer_forward(cfg, logits, x, weight, tokens=pool[i % len(pool):i % len(pool) + 1])
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            O.layer_forward(cfg, logits, x, weight, tokens=pool[i % len(pool):i % len(pool) + 1])
+        dt = time.perf_counter() - t0
+    value = args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator)", "config": workload_config(cfg),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"one token of {cfg.name} per step (routing and layout of all {cfg.T} "
+                                       f"tokens, that token's expert FFN and combine)"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":     # rank 0 alone times the oracle; no process group
+        world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+        line = run_reference(args, world, rank)
+    else:
+        world, rank, local = dist_setup(args.gpus)
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

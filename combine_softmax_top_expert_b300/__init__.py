@@ -18,7 +18,7 @@ __all__ = [
     "moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_down", "EXPORTED",
 ]
 
 library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
@@ -30,7 +30,8 @@ _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "
 
 EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
-            "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward")
+            "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
+            "moe_expert_gate_up", "moe_expert_down")
 
 
 class MoeError(RuntimeError):
@@ -95,6 +96,9 @@ def lib():
             "moe_ffn_workspace_size": (sz, [c_i64, c_i64, c_i32]),
             "moe_expert_ffn": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp, c_i64, c_vp,
                                     c_vp, sz, c_vp, c_vp]),
+            "moe_expert_gate_up": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp, c_i64, c_vp,
+                                        c_vp, c_vp, c_vp]),
+            "moe_expert_down": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_i64, c_vp, c_vp, c_vp]),
             "moe_combine": (st, [c_vp, c_i32, c_vp, c_vp, c_i64, c_i32, c_i64, c_vp, c_vp, c_i32, c_vp]),
             "moe_pack_weights": (st, [c_vp, c_vp, c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp,
                                       c_vp]),
@@ -171,6 +175,20 @@ def moe_expert_ffn(x_perm, x_scales, phys_offsets, P, phys_to_logical, rows_hint
     _check("moe_expert_ffn", lib().moe_expert_ffn(
         _p(x_perm), _p(x_scales), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w),
         _p(shared_x), T_shared, _p(y_perm), _p(ws), ws_bytes, _p(err), _s(stream)))
+
+
+def moe_expert_gate_up(x_perm, x_scales, phys_offsets, P, phys_to_logical, rows_hint, w, shared_x, T_shared, h,
+                       h_scales=None, err=None, stream=None):
+    _check("moe_expert_gate_up", lib().moe_expert_gate_up(
+        _p(x_perm), _p(x_scales), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w),
+        _p(shared_x), T_shared, _p(h), _p(h_scales), _p(err), _s(stream)))
+
+
+def moe_expert_down(h, h_scales, phys_offsets, P, phys_to_logical, rows_hint, w, T_shared, y_perm, err=None,
+                    stream=None):
+    _check("moe_expert_down", lib().moe_expert_down(
+        _p(h), _p(h_scales), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w), T_shared,
+        _p(y_perm), _p(err), _s(stream)))
 
 
 def moe_combine(y_perm, y_dt, slot_to_row, topk_w, T, k, d, shared_y, out, out_dt, stream=None):

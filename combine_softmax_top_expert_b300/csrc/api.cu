@@ -17,26 +17,27 @@ moe_status_t permute(const void *, moe_dtype_t, int64_t, int64_t, int32_t, const
 moe_status_t combine(const void *, moe_dtype_t, const int32_t *, const float *, int64_t, int32_t, int64_t,
                      const void *, void *, moe_dtype_t, cudaStream_t);
 
-constexpr size_t kTileWs = 64 * 1024;  // tile tables of the tensor-core FFN
-
-size_t ffn_ws_bytes(int64_t rows, int64_t I, moe_dtype_t dt) {
-  size_t h = 0;
-  if (dt == MOE_F32) h = (size_t)rows * I * 4;
-  else if (dt == MOE_BF16) h = (size_t)rows * I * 2;
-  else h = align_up((size_t)rows * I, 256) + (size_t)rows * (I / 128) * 4;
-  return align_up(h, 256) + kTileWs;
+size_t h_bytes(int64_t rows, int64_t I, moe_dtype_t dt) {
+  if (dt == MOE_F32) return (size_t)rows * I * 4;
+  if (dt == MOE_BF16) return (size_t)rows * I * 2;
+  return align_up((size_t)rows * I, 256) + (size_t)rows * (I / 128) * 4;
 }
 
-moe_status_t expert_ffn(const void *x_perm, const float *x_scales, const int32_t *offs, int64_t P, const int32_t *p2l,
-                        int64_t N, const moe_weights_t *w, const void *shared_x, int64_t T_shared, void *y, void *ws,
-                        size_t ws_bytes, int32_t *err, cudaStream_t st) {
+size_t ffn_ws_bytes(int64_t rows, int64_t I, moe_dtype_t dt) { return align_up(h_bytes(rows, I, dt), 256); }
+
+static moe_status_t check_ffn(const int32_t *offs, int64_t P, int64_t N, const moe_weights_t *w, int64_t T_shared) {
   if (!w || !offs || P < 1 || N < 0 || T_shared < 0) return MOE_ERR_INVALID_ARG;
   if (!w->w13 || !w->w2 || w->d <= 0 || w->I <= 0 || w->E_w < 1) return MOE_ERR_INVALID_ARG;
-  if (T_shared > 0 && (!w->has_shared || !shared_x)) return MOE_ERR_INVALID_ARG;
-  if ((N > 0 && !x_perm) || !y) return MOE_ERR_INVALID_ARG;
-  const int64_t rows = N + T_shared;
-  if (rows > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < ffn_ws_bytes(rows, w->I, w->dtype) || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (w->dtype == MOE_E4M3 && (!w->s13 || !w->s2)) return MOE_ERR_INVALID_ARG;
+  if (T_shared > 0 && !w->has_shared) return MOE_ERR_INVALID_ARG;
+  if (N + T_shared > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (w->dtype == MOE_E4M3 && T_shared > 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static FfnArgs ffn_args(const void *x_perm, const float *x_scales, const int32_t *offs, int64_t P, const int32_t *p2l,
+                        int64_t N, const moe_weights_t *w, const void *shared_x, int64_t T_shared, void *h,
+                        float *h_scales, void *y, int32_t *err) {
   FfnArgs a;
   a.x_perm = x_perm;
   a.x_scales = x_scales;
@@ -47,27 +48,46 @@ moe_status_t expert_ffn(const void *x_perm, const float *x_scales, const int32_t
   a.w = w;
   a.shared_x = shared_x;
   a.T_shared = T_shared;
-  a.h = ws;
-  a.h_scales = nullptr;
-  size_t hbytes;
-  if (w->dtype == MOE_E4M3) {
-    a.h_scales = reinterpret_cast<float *>(static_cast<char *>(ws) + align_up((size_t)rows * w->I, 256));
-    hbytes = align_up((size_t)rows * w->I, 256) + (size_t)rows * (w->I / 128) * 4;
-  } else {
-    hbytes = (size_t)rows * w->I * (w->dtype == MOE_F32 ? 4 : 2);
-  }
-  a.tiles = static_cast<char *>(ws) + align_up(hbytes, 256);
+  a.h = h;
+  a.h_scales = h_scales;
   a.y = y;
   a.err = err;
-  switch (w->dtype) {
-    case MOE_F32: return ffn_f32(a, st);
-    case MOE_BF16: return ffn_bf16(a, st);
-    case MOE_E4M3:
-      if (N > 0 && !x_scales) return MOE_ERR_INVALID_ARG;
-      if (T_shared > 0) return MOE_ERR_UNSUPPORTED;
-      return ffn_e4m3(a, st);
+  return a;
+}
+
+moe_status_t gate_up(const FfnArgs &a, cudaStream_t st) {
+  switch (a.w->dtype) {
+    case MOE_F32: return gate_up_f32(a, st);
+    case MOE_BF16: return gate_up_bf16(a, st);
+    case MOE_E4M3: return gate_up_e4m3(a, st);
   }
   return MOE_ERR_INVALID_ARG;
+}
+
+moe_status_t down(const FfnArgs &a, cudaStream_t st) {
+  switch (a.w->dtype) {
+    case MOE_F32: return down_f32(a, st);
+    case MOE_BF16: return down_bf16(a, st);
+    case MOE_E4M3: return down_e4m3(a, st);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status_t expert_ffn(const void *x_perm, const float *x_scales, const int32_t *offs, int64_t P, const int32_t *p2l,
+                        int64_t N, const moe_weights_t *w, const void *shared_x, int64_t T_shared, void *y, void *ws,
+                        size_t ws_bytes, int32_t *err, cudaStream_t st) {
+  moe_status_t r = check_ffn(offs, P, N, w, T_shared);
+  if (r != MOE_OK) return r;
+  if ((N > 0 && !x_perm) || (T_shared > 0 && !shared_x) || !y) return MOE_ERR_INVALID_ARG;
+  if (w->dtype == MOE_E4M3 && N > 0 && !x_scales) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = N + T_shared;
+  if (!ws || ws_bytes < ffn_ws_bytes(rows, w->I, w->dtype) || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  float *hs = w->dtype == MOE_E4M3
+                  ? reinterpret_cast<float *>(static_cast<char *>(ws) + align_up((size_t)rows * w->I, 256))
+                  : nullptr;
+  const FfnArgs a = ffn_args(x_perm, x_scales, offs, P, p2l, N, w, shared_x, T_shared, ws, hs, y, err);
+  if ((r = gate_up(a, st)) != MOE_OK) return r;
+  return down(a, st);
 }
 
 // ------------------------------------------------------------------ layer forward
@@ -155,6 +175,30 @@ MOE_API moe_status_t moe_expert_ffn(const void *x_perm, const float *x_scales, c
                                     int32_t *err, moe_stream_t stream) {
   return expert_ffn(x_perm, x_scales, phys_offsets, P, phys_to_logical, rows_hint, w, shared_x, T_shared, y_perm, ws,
                     ws_bytes, err, as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_expert_gate_up(const void *x_perm, const float *x_scales, const int32_t *phys_offsets,
+                                        int64_t P, const int32_t *phys_to_logical, int64_t rows_hint,
+                                        const moe_weights_t *w, const void *shared_x, int64_t T_shared, void *h,
+                                        float *h_scales, int32_t *err, moe_stream_t stream) {
+  moe_status_t r = check_ffn(phys_offsets, P, rows_hint, w, T_shared);
+  if (r != MOE_OK) return r;
+  if ((rows_hint > 0 && !x_perm) || (T_shared > 0 && !shared_x) || !h) return MOE_ERR_INVALID_ARG;
+  if (w->dtype == MOE_E4M3 && ((rows_hint > 0 && !x_scales) || !h_scales)) return MOE_ERR_INVALID_ARG;
+  return gate_up(ffn_args(x_perm, x_scales, phys_offsets, P, phys_to_logical, rows_hint, w, shared_x, T_shared, h,
+                          h_scales, nullptr, err),
+                 as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_expert_down(const void *h, const float *h_scales, const int32_t *phys_offsets, int64_t P,
+                                     const int32_t *phys_to_logical, int64_t rows_hint, const moe_weights_t *w,
+                                     int64_t T_shared, void *y_perm, int32_t *err, moe_stream_t stream) {
+  moe_status_t r = check_ffn(phys_offsets, P, rows_hint, w, T_shared);
+  if (r != MOE_OK) return r;
+  if (!h || !y_perm || (w->dtype == MOE_E4M3 && !h_scales)) return MOE_ERR_INVALID_ARG;
+  return down(ffn_args(nullptr, nullptr, phys_offsets, P, phys_to_logical, rows_hint, w, nullptr, T_shared,
+                       const_cast<void *>(h), const_cast<float *>(h_scales), y_perm, err),
+              as_cuda(stream));
 }
 
 MOE_API size_t moe_layer_workspace_size(const moe_shape_t *shape) {

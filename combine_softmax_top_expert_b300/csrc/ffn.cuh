@@ -16,7 +16,6 @@ struct FfnArgs {
   int64_t T_shared;
   void *h;                 // [N + T_shared, I] workspace (+ e4m3 scales after it)
   float *h_scales;         // e4m3: [N + T_shared, I/128]
-  void *tiles;             // scheduling workspace
   void *y;                 // [N + T_shared, d]
   int32_t *err;
 };
@@ -32,8 +31,12 @@ __device__ __forceinline__ int group_of_row(const int32_t *offs, int P, int row)
   return lo;
 }
 
-moe_status_t ffn_f32(const FfnArgs &a, cudaStream_t st);
-moe_status_t ffn_bf16(const FfnArgs &a, cudaStream_t st);
-moe_status_t ffn_e4m3(const FfnArgs &a, cudaStream_t st);
+// The two phases of the expert FFN: h = silu(x W_gate) * (x W_up), then y = h W_down.
+moe_status_t gate_up_f32(const FfnArgs &a, cudaStream_t st);
+moe_status_t down_f32(const FfnArgs &a, cudaStream_t st);
+moe_status_t gate_up_bf16(const FfnArgs &a, cudaStream_t st);
+moe_status_t down_bf16(const FfnArgs &a, cudaStream_t st);
+moe_status_t gate_up_e4m3(const FfnArgs &a, cudaStream_t st);
+moe_status_t down_e4m3(const FfnArgs &a, cudaStream_t st);
 
 }  // namespace moe

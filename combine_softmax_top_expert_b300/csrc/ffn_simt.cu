@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) down_f32_kernel(SimtArgs a) {
 
 }  // namespace
 
-moe_status_t ffn_f32(const FfnArgs &f, cudaStream_t st) {
+static SimtArgs simt_args(const FfnArgs &f) {
   SimtArgs a;
   a.x_perm = static_cast<const float *>(f.x_perm);
   a.shared_x = static_cast<const float *>(f.shared_x);
@@ -93,10 +93,22 @@ moe_status_t ffn_f32(const FfnArgs &f, cudaStream_t st) {
   a.h = static_cast<float *>(f.h);
   a.y = static_cast<float *>(f.y);
   a.err = f.err;
+  return a;
+}
+
+moe_status_t gate_up_f32(const FfnArgs &f, cudaStream_t st) {
+  const SimtArgs a = simt_args(f);
   if (a.rows == 0) return MOE_OK;
-  const int64_t n1 = a.rows * a.I, n2 = a.rows * a.d;
-  gateup_f32_kernel<<<(unsigned)((n1 + 255) / 256), 256, 0, st>>>(a);
-  down_f32_kernel<<<(unsigned)((n2 + 255) / 256), 256, 0, st>>>(a);
+  const int64_t n = a.rows * a.I;
+  gateup_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  return launch_status();
+}
+
+moe_status_t down_f32(const FfnArgs &f, cudaStream_t st) {
+  const SimtArgs a = simt_args(f);
+  if (a.rows == 0) return MOE_OK;
+  const int64_t n = a.rows * a.d;
+  down_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   return launch_status();
 }
 

@@ -401,31 +401,24 @@ bool use_swap(int64_t N, int64_t P) {
   return N < 64 * P;
 }
 
-}  // namespace
+// Maps and parameters shared by both phases.
+struct Plan {
+  GemmParams p;
+  bool swap;
+  int kbw;
+  uint32_t tok_box;
+};
 
-moe_status_t ffn_bf16(const FfnArgs &f, cudaStream_t st) {
+moe_status_t plan_bf16(const FfnArgs &f, Plan *pl) {
   const moe_weights_t &w = *f.w;
-  const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
+  const int64_t d = w.d, I = w.I;
   if (d % 128 || I % 128 || f.P > 2048) return MOE_ERR_UNSUPPORTED;
-  if (w.E_w * 2 * I > INT32_MAX || rows * d > INT64_MAX / 4) return MOE_ERR_UNSUPPORTED;
-  if (rows == 0) return MOE_OK;
-  const bool swap = use_swap(f.N + f.T_shared, f.P);
-  const uint32_t tok_box = swap ? 16 : 128;
-  CUtensorMap m_x, m_sh, m_w13, m_h, m_w2;
-  const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
-  const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
-  if (!make_map(&m_x, xsrc, xrows, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
-  if (f.T_shared > 0) {
-    if (!make_map(&m_sh, f.shared_x, f.T_shared, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
-  } else {
-    m_sh = m_x;
-  }
-  const int kbw = (d % 256 == 0) ? 256 : 128;
-  if (!make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * I, d, 2, 128)) return MOE_ERR_INVALID_ARG;
-  if (!make_map(&m_h, f.h, rows, I, 2, tok_box)) return MOE_ERR_INVALID_ARG;
-  if (!make_map(&m_w2, w.w2, (uint64_t)w.E_w * d, I, 2, swap ? 128 : kbw)) return MOE_ERR_INVALID_ARG;
-
-  GemmParams p{};
+  if (w.E_w * 2 * I > INT32_MAX || w.E_w * d > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  pl->swap = use_swap(f.N + f.T_shared, f.P);
+  pl->tok_box = pl->swap ? 16 : 128;
+  pl->kbw = (d % 256 == 0) ? 256 : 128;
+  GemmParams &p = pl->p;
+  p = GemmParams{};
   p.offs = f.offs;
   p.p2l = f.p2l;
   p.P = (int)f.P;
@@ -433,28 +426,61 @@ moe_status_t ffn_bf16(const FfnArgs &f, cudaStream_t st) {
   p.T_shared = (int)f.T_shared;
   p.E_w = (int)w.E_w;
   p.err = f.err;
-  // gate/up
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
+  Plan pl;
+  moe_status_t s = plan_bf16(f, &pl);
+  if (s != MOE_OK) return s;
+  const moe_weights_t &w = *f.w;
+  const int64_t d = w.d, I = w.I;
+  if (f.N + f.T_shared == 0) return MOE_OK;
+  CUtensorMap m_x, m_sh, m_w13;
+  const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
+  const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
+  if (!make_map(&m_x, xsrc, xrows, d, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
+  if (f.T_shared > 0) {
+    if (!make_map(&m_sh, f.shared_x, f.T_shared, d, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
+  } else {
+    m_sh = m_x;
+  }
+  if (!make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * I, d, 2, 128)) return MOE_ERR_INVALID_ARG;
+  GemmParams p = pl.p;
   p.feat = (int)I;
   p.K = (int)d;
   p.w_rows = (int)(2 * I);
   p.shared_row0 = 0;
   p.out = static_cast<uint16_t *>(f.h);
   p.ld = I;
-  moe_status_t s = swap ? launch<true, true, 128>(p, m_x, m_sh, m_w13, st)
-                        : launch<true, false, 128>(p, m_x, m_sh, m_w13, st);
+  return pl.swap ? launch<true, true, 128>(p, m_x, m_sh, m_w13, st) : launch<true, false, 128>(p, m_x, m_sh, m_w13, st);
+}
+
+moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
+  Plan pl;
+  moe_status_t s = plan_bf16(f, &pl);
   if (s != MOE_OK) return s;
-  // down
+  const moe_weights_t &w = *f.w;
+  const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
+  if (rows == 0) return MOE_OK;
+  CUtensorMap m_h, m_w2;
+  if (!make_map(&m_h, f.h, rows, I, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
+  if (!make_map(&m_w2, w.w2, (uint64_t)w.E_w * d, I, 2, pl.swap ? 128 : pl.kbw)) return MOE_ERR_INVALID_ARG;
+  GemmParams p = pl.p;
   p.feat = (int)d;
   p.K = (int)I;
   p.w_rows = (int)d;
   p.shared_row0 = (int)f.N;
   p.out = static_cast<uint16_t *>(f.y);
   p.ld = d;
-  if (swap) return launch<false, true, 128>(p, m_h, m_h, m_w2, st);
-  return kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, m_w2, st)
-                    : launch<false, false, 128>(p, m_h, m_h, m_w2, st);
+  if (pl.swap) return launch<false, true, 128>(p, m_h, m_h, m_w2, st);
+  return pl.kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, m_w2, st) : launch<false, false, 128>(p, m_h, m_h, m_w2, st);
 }
 
-moe_status_t ffn_e4m3(const FfnArgs &, cudaStream_t) { return MOE_ERR_UNSUPPORTED; }
+moe_status_t gate_up_e4m3(const FfnArgs &, cudaStream_t) { return MOE_ERR_UNSUPPORTED; }
+moe_status_t down_e4m3(const FfnArgs &, cudaStream_t) { return MOE_ERR_UNSUPPORTED; }
+
 
 }  // namespace moe

@@ -213,13 +213,36 @@ size_t moe_ffn_workspace_size(int64_t rows, int64_t I, moe_dtype_t expert_dtype)
  * block scales; h quantised per row per 128 channels (same rule as moe_permute);
  * y bf16.  `rows_hint` is the number of routed rows N (phys_offsets[P] on the
  * device must equal it).  ws: moe_ffn_workspace_size(N + T_shared, I, dtype).
- * Limits (tensor-core paths): d % 128 == 0, I % 128 == 0. */
+ * Limits (tensor-core paths): d % 128 == 0, I % 128 == 0, P <= 2048.  The tile
+ * orientation follows the rows per expert; MOE_B300_FFN_TILES=swap|wide in the
+ * environment forces one (both give the same results within rounding). */
 moe_status_t moe_expert_ffn(const void *x_perm, const float *x_scales,
                             const int32_t *phys_offsets, int64_t P,
                             const int32_t *phys_to_logical, int64_t rows_hint,
                             const moe_weights_t *w, const void *shared_x,
                             int64_t T_shared, void *y_perm, void *ws,
                             size_t ws_bytes, int32_t *err, moe_stream_t stream);
+
+/* The expert FFN's first phase on its own ("6.4 ...", section 2.1, the gate and
+ * up matrices): h = silu(x W_gate[e]) * (x W_up[e]) for every row of every
+ * physical expert (and the shared expert's T_shared rows after row N), as in
+ * moe_expert_ffn.  h [N + T_shared, I]: fp32 (f32 weights), bf16, or e4m3 with
+ * h_scales [N + T_shared, I/128] (per row per 128 channels, the moe_permute rule). */
+moe_status_t moe_expert_gate_up(const void *x_perm, const float *x_scales,
+                                const int32_t *phys_offsets, int64_t P,
+                                const int32_t *phys_to_logical, int64_t rows_hint,
+                                const moe_weights_t *w, const void *shared_x,
+                                int64_t T_shared, void *h, float *h_scales,
+                                int32_t *err, moe_stream_t stream);
+
+/* The expert FFN's second phase on its own ("6.4 ...", section 2.1, the down
+ * matrix): y = h W_down[e] for the rows moe_expert_gate_up wrote.  y_perm
+ * [N + T_shared, d]: fp32 for f32 weights, else bf16. */
+moe_status_t moe_expert_down(const void *h, const float *h_scales,
+                             const int32_t *phys_offsets, int64_t P,
+                             const int32_t *phys_to_logical, int64_t rows_hint,
+                             const moe_weights_t *w, int64_t T_shared, void *y_perm,
+                             int32_t *err, moe_stream_t stream);
 
 /* Combine ("6.4 ...", section 3.1, step 4: weighted-sum by route weights).
  * out[t] = sum_{j<k} topk_w[t, j] * y_perm[slot_to_row[t, j]] (+ shared_y[t]),
