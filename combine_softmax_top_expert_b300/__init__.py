@@ -18,20 +18,22 @@ __all__ = [
     "moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "moe_expert_gate_up", "moe_expert_down", "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "EXPORTED",
+    "MOE_DISPATCH_STATIC_SCRATCH_BYTES",
 ]
 
 library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
 
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_DEV_NONFINITE_LOGIT, MOE_DEV_ID_RANGE, MOE_DEV_TIMEOUT, MOE_DEV_LAYOUT = 1, 2, 4, 8
+MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 << 20
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
 
 EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-            "moe_expert_gate_up", "moe_expert_down")
+            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static")
 
 
 class MoeError(RuntimeError):
@@ -92,6 +94,8 @@ def lib():
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
             "moe_dispatch_layout": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
                                     + [c_vp, sz, c_vp, c_vp]),
+            "moe_dispatch_layout_static": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
+                                           + [c_vp, c_vp]),
             "moe_permute": (st, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp]),
             "moe_ffn_workspace_size": (sz, [c_i64, c_i64, c_i32]),
             "moe_expert_ffn": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp, c_i64, c_vp,
@@ -159,6 +163,17 @@ def moe_dispatch_layout(topk_ids, T, k, E, R, eplb, logical_counts, phys_counts,
     _check("moe_dispatch_layout", lib().moe_dispatch_layout(
         _p(topk_ids), T, k, E, R, ep, _p(logical_counts), _p(phys_counts), _p(phys_offsets), _p(rank_counts),
         _p(rank_offsets), _p(row_to_token), _p(slot_to_row), _p(stats), _p(ws), ws_bytes, _p(err), _s(stream)))
+
+
+def moe_dispatch_layout_static(topk_ids, T, k, E, R, eplb, logical_counts, phys_counts, phys_offsets, rank_counts,
+                               rank_offsets, row_to_token, slot_to_row, stats, err=None, stream=None):
+    """moe_dispatch_layout without a workspace argument: for callers that cannot
+    allocate device memory, the library's built-in scratch array is used (see
+    include/moe.h for the size limit and the one-call-at-a-time rule)."""
+    ep = ctypes.byref(eplb) if eplb is not None else None
+    _check("moe_dispatch_layout_static", lib().moe_dispatch_layout_static(
+        _p(topk_ids), T, k, E, R, ep, _p(logical_counts), _p(phys_counts), _p(phys_offsets), _p(rank_counts),
+        _p(rank_offsets), _p(row_to_token), _p(slot_to_row), _p(stats), _p(err), _s(stream)))
 
 
 def moe_permute(x, x_dt, T, d, k, slot_to_row, x_perm, perm_dt, perm_scales=None, stream=None):

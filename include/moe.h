@@ -144,6 +144,36 @@ moe_status_t moe_route(const float *logits, int64_t T, int64_t E, int32_t k,
                        int32_t *topk_ids, float *topk_w, int32_t *err,
                        moe_stream_t stream);
 
+/* Size of the scratch array built into the library for moe_dispatch_layout_static. */
+#define MOE_DISPATCH_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* moe_dispatch_layout for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a deployment convenience of this library).  Some
+ * callers receive only their input and output buffers and have no device
+ * allocator to take a workspace from -- a plugin whose host runtime owns and
+ * pre-budgets all memory, or a latency-critical path where allocating is not
+ * allowed.  This entry point computes exactly what moe_dispatch_layout computes
+ * (same arguments and results, minus ws/ws_bytes) and allocates nothing: its
+ * scratch is a MOE_DISPATCH_STATIC_SCRATCH_BYTES array inside the library, which
+ * every GPU that loads the library reserves until the process exits.
+ *   - Returns MOE_ERR_WORKSPACE, queuing nothing, when the batch needs more
+ *     scratch than that, i.e. moe_dispatch_workspace_size(T, k, P) >
+ *     MOE_DISPATCH_STATIC_SCRATCH_BYTES (about 900k slots T*k at P = 256,
+ *     500k at P = 2048).
+ *   - All calls share the one array and it keeps the previous call's contents;
+ *     the kernels overwrite each entry before reading it.  Calls whose work
+ *     overlaps on a GPU (different streams or host threads) race on it and give
+ *     wrong results: keep them on one stream or synchronise in between.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture. */
+moe_status_t moe_dispatch_layout_static(const int32_t *topk_ids, int64_t T, int32_t k,
+                                        int64_t E, int32_t R, const moe_eplb_t *eplb,
+                                        int32_t *logical_counts, int32_t *phys_counts,
+                                        int32_t *phys_offsets, int32_t *rank_counts,
+                                        int32_t *rank_offsets, int32_t *row_to_token,
+                                        int32_t *slot_to_row, moe_load_stats_t *stats,
+                                        int32_t *err, moe_stream_t stream);
+
 /* EPLB one-step replica map ("6.4 ...", section 5.3: (experts + redundant)/EP
  * physical experts per card; "How Expert Parallelism Works for Mixture-of-Experts
  * Models in vLLM", "MoE Layer Construction": num_physical = E + redundant).
