@@ -18,7 +18,7 @@ __all__ = [
     "moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error", "EXPORTED",
     "MOE_DISPATCH_STATIC_SCRATCH_BYTES",
 ]
 
@@ -33,7 +33,7 @@ _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "
 EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static")
+            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error")
 
 
 class MoeError(RuntimeError):
@@ -89,6 +89,7 @@ def lib():
         sz, st = ctypes.c_size_t, c_i32
         sig = {
             "moe_status_string": (ctypes.c_char_p, [st]),
+            "moe_last_cuda_error": (ctypes.c_char_p, []),
             "moe_route": (st, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
@@ -135,7 +136,14 @@ def _s(stream):
 
 def _check(name, status):
     if status != 0:
-        raise MoeError(name, status)
+        err = MoeError(name, status)
+        if status == 4:
+            err.args = (err.args[0] + ": " + moe_last_cuda_error(),)
+        raise err
+
+
+def moe_last_cuda_error() -> str:
+    return lib().moe_last_cuda_error().decode()
 
 
 # ------------------------------------------------------------------ entry points

@@ -153,6 +153,16 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
 
 using namespace moe;
 
+cudaError_t &moe::last_cuda_error() {
+  static thread_local cudaError_t e = cudaSuccess;
+  return e;
+}
+
+MOE_API const char *moe_last_cuda_error(void) {
+  const cudaError_t e = last_cuda_error();
+  return e == cudaSuccess ? "" : cudaGetErrorString(e);
+}
+
 MOE_API const char *moe_status_string(moe_status_t s) {
   switch (s) {
     case MOE_OK: return "ok";

@@ -16,10 +16,16 @@ constexpr unsigned kFull = 0xffffffffu;
 
 inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
-inline moe_status_t launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+// The last CUDA error a call of this library saw on the calling thread.
+cudaError_t &last_cuda_error();
+
+inline moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  last_cuda_error() = e;
+  return MOE_ERR_CUDA;
 }
+
+inline moe_status_t launch_status() { return cuda_status(cudaGetLastError()); }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

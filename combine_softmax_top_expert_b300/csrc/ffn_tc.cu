@@ -1,6 +1,6 @@
-// Grouped SwiGLU expert FFN on the tcgen05 tensor cores ("6.4 Data parallelism
-// and expert parallelism", section 2.1: gate, up, down; section 7: the shared
-// expert is one more always-on group).
+// Grouped SwiGLU expert FFN on the tcgen05 tensor cores, bf16 ("6.4 Data
+// parallelism and expert parallelism", section 2.1: gate, up, down; section 7:
+// the shared expert is one more always-on group).
 //
 // Two launches per forward, each a persistent grouped GEMM over all experts:
 //   gate/up   h = silu(X W_gate) * (X W_up)   (SwiGLU fused in the epilogue, bf16 h)
@@ -17,21 +17,16 @@
 //   swap  A = 128 weight rows (gate and up as two MMAs), B = up to 32 token rows:
 //         D is features x tokens, so a group of a few tokens streams its weights
 //         at HBM speed without padding tokens to 128.  For decode-sized batches.
-#include <cudaTypedefs.h>
-
-#include <cstdlib>
-#include <cstring>
-
-#include "ffn.cuh"
-#include "tc.cuh"
+#include "grouped.cuh"
 
 namespace moe {
 namespace {
 
 using namespace tc;
+using grouped::Params;
+using grouped::Tile;
 
 constexpr int kThreads = 192;
-constexpr int kMaxGroups = 2048 + 1;
 
 template <bool kGated, bool kSwap, int kBW>
 struct Cfg {
@@ -45,101 +40,15 @@ struct Cfg {
   static constexpr int kTokTile = kSwap ? 32 : 128;
   static constexpr int kFeatTile = kSwap ? 128 : (kGated ? 128 : kBW);
   static constexpr int kBars = 2 * kStages + 5;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kBars * 8 + 16 + (kMaxGroups + 1) * 4;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * kStage + kBars * 8 + 16 + (grouped::kMaxGroups + 1) * 4;
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-struct GemmParams {
-  const int32_t *offs;  // [P + 1]
-  const int32_t *p2l;   // [P] or null
-  int P, N, T_shared, E_w;
-  int feat;             // output features: I (gate/up) or d (down)
-  int K;                // reduction length: d (gate/up) or I (down)
-  int w_rows;           // weight rows per expert: 2I (gate/up) or d (down)
-  int shared_row0;      // row of the shared group's first token in its token map
-  uint16_t *out;        // h [rows, I] or y [rows, d], bf16
-  int64_t ld;
-  int32_t *err;
-};
-
-struct Tile {
-  int e, tok_row, out_row, valid, nt;
-  bool shared;
-};
-
-__device__ __forceinline__ void group_span(const GemmParams &p, int g, int *r0, int *n) {
-  if (g < p.P) {
-    const int a = min(max(p.offs[g], 0), p.N);
-    const int b = min(max(p.offs[g + 1], 0), p.N);
-    *r0 = a;
-    *n = max(b - a, 0);
-  } else {
-    *r0 = 0;
-    *n = p.T_shared;
-  }
-}
-
-// In-place inclusive scan of a[0..n) by the whole block.
-__device__ void block_scan(int *a, int n) {
-  __shared__ int wsum[kThreads / 32];
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
-  int s = 0;
-  for (int i = lo; i < hi; ++i) s += a[i];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int v = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += t;
-  }
-  if (lane == 31) wsum[warp] = v;
-  __syncthreads();
-  int off = v - s;
-  for (int w = 0; w < warp; ++w) off += wsum[w];
-  for (int i = lo; i < hi; ++i) {
-    off += a[i];
-    a[i] = off;
-  }
-  __syncthreads();
-}
-
-template <class C>
-__device__ __forceinline__ Tile decode(const GemmParams &p, const int *tile_start, int G, int NT, int tile) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tile_start[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  const int g = lo, local = tile - tile_start[g];
-  int r0, n;
-  group_span(p, g, &r0, &n);
-  const int MT = (n + C::kTokTile - 1) / C::kTokTile;
-  int mt, nt;
-  if (C::kTokTile == 32) {  // swap: token tiles of one feature block run back to back
-    nt = local / MT;
-    mt = local % MT;
-  } else {                  // wide: feature blocks of one token tile run back to back
-    mt = local / NT;
-    nt = local % NT;
-  }
-  Tile t;
-  t.shared = g >= p.P;
-  int e = t.shared ? p.E_w - 1 : (p.p2l ? p.p2l[g] : g);
-  if (e < 0 || e >= p.E_w) e = -1;
-  t.e = e;
-  t.nt = nt;
-  t.valid = min(C::kTokTile, n - mt * C::kTokTile);
-  t.tok_row = (t.shared ? p.shared_row0 : r0) + mt * C::kTokTile;
-  t.out_row = (t.shared ? p.N : r0) + mt * C::kTokTile;
-  return t;
-}
-
 template <bool kGated, bool kSwap, int kBW>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_bf16(const GemmParams p, const __grid_constant__ CUtensorMap tm_tok,
+    grouped_gemm_bf16(const Params p, const __grid_constant__ CUtensorMap tm_tok,
                       const __grid_constant__ CUtensorMap tm_sh, const __grid_constant__ CUtensorMap tm_w) {
   using C = Cfg<kGated, kSwap, kBW>;
   extern __shared__ uint8_t smem_raw[];
@@ -153,6 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull = [&](int b) { return smem_u32(&bars[2 * C::kStages + b]); };
   auto tempty = [&](int b) { return smem_u32(&bars[2 * C::kStages + 2 + b]); };
   const uint32_t drain = smem_u32(&bars[2 * C::kStages + 4]);
+  uint16_t *out = static_cast<uint16_t *>(p.out);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.P + (p.T_shared > 0 ? 1 : 0);
@@ -181,14 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&misc[0]), C::kTmemCols);
     tmem_relinquish();
   }
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
-    int r0, n;
-    group_span(p, g, &r0, &n);
-    tile_start[g + 1] = n > 0 ? ((n + C::kTokTile - 1) / C::kTokTile) * NT : 0;
-  }
-  if (threadIdx.x == 0) tile_start[0] = 0;
-  __syncthreads();
-  block_scan(tile_start + 1, G);
+  grouped::build_tile_table<C::kTokTile>(p, tile_start, G, NT);
   fence_before();
   __syncthreads();
   fence_after();
@@ -201,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0, issued = 0;
     uint32_t ph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode<C>(p, tile_start, G, NT, tile);
+      const Tile t = grouped::decode<C::kTokTile>(p, tile_start, G, NT, tile);
       const CUtensorMap *tmt = (kGated && t.shared) ? &tm_sh : &tm_tok;
       const int nb = kSwap ? (t.valid + 15) / 16 : 0;
       const uint32_t bytes = C::kABytes + (kSwap ? nb * 2048 : C::kBBytes);
@@ -241,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0, it = 0;
     uint32_t ph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const Tile t = decode<C>(p, tile_start, G, NT, tile);
+      const Tile t = grouped::decode<C::kTokTile>(p, tile_start, G, NT, tile);
       const int b = it & 1;
       if (!mbar_wait(tempty(b), ((it >> 1) & 1) ^ 1, abort_flag, p.err)) break;
       fence_after();
@@ -281,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;  // TMEM lane: token row (wide) or feature (swap)
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const Tile t = decode<C>(p, tile_start, G, NT, tile);
+      const Tile t = grouped::decode<C::kTokTile>(p, tile_start, G, NT, tile);
       const int b = it & 1;
       if (!mbar_wait(tfull(b), (it >> 1) & 1, abort_flag, p.err)) break;
       fence_after();
@@ -289,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * C::kAccCols;
       if (!kSwap) {
         const bool ok = r < t.valid && t.e >= 0;
-        uint16_t *orow = p.out + (int64_t)(t.out_row + (ok ? r : 0)) * p.ld + (int64_t)t.nt * C::kFeatTile;
+        uint16_t *orow = out + (int64_t)(t.out_row + (ok ? r : 0)) * p.ld + (int64_t)t.nt * C::kFeatTile;
         constexpr int kChunks = kGated ? 4 : kBW / 32;
 #pragma unroll 1
         for (int c = 0; c < kChunks; ++c) {
@@ -319,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kGated) tmem_ld32(tb + 32, u);
         tmem_wait_ld();
         if (t.e >= 0) {
-          uint16_t *col = p.out + (int64_t)t.out_row * p.ld + (int64_t)t.nt * 128 + r;
+          uint16_t *col = out + (int64_t)t.out_row * p.ld + (int64_t)t.nt * 128 + r;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (c < t.valid) {
@@ -342,145 +245,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }();
-  return fn;
-}
-
-// 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements; boxes of
-// box_rows x (128 / esize) elements, 128-byte swizzle, zero fill outside.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, int esize, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn || !base || rows == 0 || !aligned(base, 16) || (cols * esize) % 16) return false;
-  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * (uint64_t)esize};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / esize), box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                 cudaSuccess)
-    return 0;
-  return n;
-}
-
 template <bool kGated, bool kSwap, int kBW>
-moe_status_t launch(const GemmParams &p, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
                     cudaStream_t st) {
   using Cf = Cfg<kGated, kSwap, kBW>;
   auto k = grouped_gemm_bf16<kGated, kSwap, kBW>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem) != cudaSuccess)
+  if (cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem)) != MOE_OK)
     return MOE_ERR_CUDA;
-  const int grid = sm_count();
+  const int grid = grouped::sm_count();
   if (grid <= 0) return MOE_ERR_CUDA;
   k<<<grid, kThreads, Cf::kSmem, st>>>(p, a, b, c);
   return launch_status();
 }
 
-// Tile orientation: "swap" for few rows per expert, "wide" otherwise; the
-// environment variable MOE_B300_FFN_TILES=swap|wide overrides the choice.
-bool use_swap(int64_t N, int64_t P) {
-  const char *env = std::getenv("MOE_B300_FFN_TILES");
-  if (env && !std::strcmp(env, "swap")) return true;
-  if (env && !std::strcmp(env, "wide")) return false;
-  return N < 64 * P;
-}
-
-// Maps and parameters shared by both phases.
-struct Plan {
-  GemmParams p;
-  bool swap;
-  int kbw;
-  uint32_t tok_box;
-};
-
-moe_status_t plan_bf16(const FfnArgs &f, Plan *pl) {
+moe_status_t check_bf16(const FfnArgs &f) {
   const moe_weights_t &w = *f.w;
-  const int64_t d = w.d, I = w.I;
-  if (d % 128 || I % 128 || f.P > 2048) return MOE_ERR_UNSUPPORTED;
-  if (w.E_w * 2 * I > INT32_MAX || w.E_w * d > INT32_MAX) return MOE_ERR_UNSUPPORTED;
-  pl->swap = use_swap(f.N + f.T_shared, f.P);
-  pl->tok_box = pl->swap ? 16 : 128;
-  pl->kbw = (d % 256 == 0) ? 256 : 128;
-  GemmParams &p = pl->p;
-  p = GemmParams{};
-  p.offs = f.offs;
-  p.p2l = f.p2l;
-  p.P = (int)f.P;
-  p.N = (int)f.N;
-  p.T_shared = (int)f.T_shared;
-  p.E_w = (int)w.E_w;
-  p.err = f.err;
+  if (w.d % 128 || w.I % 128 || f.P > 2048) return MOE_ERR_UNSUPPORTED;
+  if (w.E_w * 2 * w.I > INT32_MAX || w.E_w * w.d > INT32_MAX) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
 }  // namespace
 
 moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
-  Plan pl;
-  moe_status_t s = plan_bf16(f, &pl);
+  moe_status_t s = check_bf16(f);
   if (s != MOE_OK) return s;
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I;
   if (f.N + f.T_shared == 0) return MOE_OK;
+  const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
+  const uint32_t tok_box = swap ? 16 : 128;
   CUtensorMap m_x, m_sh, m_w13;
   const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
   const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
-  if (!make_map(&m_x, xsrc, xrows, d, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_map(&m_x, xsrc, xrows, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
   if (f.T_shared > 0) {
-    if (!make_map(&m_sh, f.shared_x, f.T_shared, d, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
+    if (!grouped::make_map(&m_sh, f.shared_x, f.T_shared, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
   } else {
     m_sh = m_x;
   }
-  if (!make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * I, d, 2, 128)) return MOE_ERR_INVALID_ARG;
-  GemmParams p = pl.p;
+  if (!grouped::make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * I, d, 2, 128)) return MOE_ERR_INVALID_ARG;
+  Params p = grouped::base_params(f);
   p.feat = (int)I;
   p.K = (int)d;
   p.w_rows = (int)(2 * I);
   p.shared_row0 = 0;
-  p.out = static_cast<uint16_t *>(f.h);
+  p.out = f.h;
   p.ld = I;
-  return pl.swap ? launch<true, true, 128>(p, m_x, m_sh, m_w13, st) : launch<true, false, 128>(p, m_x, m_sh, m_w13, st);
+  return swap ? launch<true, true, 128>(p, m_x, m_sh, m_w13, st) : launch<true, false, 128>(p, m_x, m_sh, m_w13, st);
 }
 
 moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
-  Plan pl;
-  moe_status_t s = plan_bf16(f, &pl);
+  moe_status_t s = check_bf16(f);
   if (s != MOE_OK) return s;
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
   if (rows == 0) return MOE_OK;
+  const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
+  const int kbw = (d % 256 == 0) ? 256 : 128;
   CUtensorMap m_h, m_w2;
-  if (!make_map(&m_h, f.h, rows, I, 2, pl.tok_box)) return MOE_ERR_INVALID_ARG;
-  if (!make_map(&m_w2, w.w2, (uint64_t)w.E_w * d, I, 2, pl.swap ? 128 : pl.kbw)) return MOE_ERR_INVALID_ARG;
-  GemmParams p = pl.p;
+  if (!grouped::make_map(&m_h, f.h, rows, I, 2, swap ? 16 : 128)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_map(&m_w2, w.w2, (uint64_t)w.E_w * d, I, 2, swap ? 128 : kbw)) return MOE_ERR_INVALID_ARG;
+  Params p = grouped::base_params(f);
   p.feat = (int)d;
   p.K = (int)I;
   p.w_rows = (int)d;
   p.shared_row0 = (int)f.N;
-  p.out = static_cast<uint16_t *>(f.y);
+  p.out = f.y;
   p.ld = d;
-  if (pl.swap) return launch<false, true, 128>(p, m_h, m_h, m_w2, st);
-  return pl.kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, m_w2, st) : launch<false, false, 128>(p, m_h, m_h, m_w2, st);
+  if (swap) return launch<false, true, 128>(p, m_h, m_h, m_w2, st);
+  return kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, m_w2, st) : launch<false, false, 128>(p, m_h, m_h, m_w2, st);
 }
-
-moe_status_t gate_up_e4m3(const FfnArgs &, cudaStream_t) { return MOE_ERR_UNSUPPORTED; }
-moe_status_t down_e4m3(const FfnArgs &, cudaStream_t) { return MOE_ERR_UNSUPPORTED; }
-
 
 }  // namespace moe

@@ -1,0 +1,189 @@
+// Tile scheduling and TMA descriptors shared by the grouped expert GEMMs.
+//
+// A grouped GEMM runs over groups: the P physical experts (rows offs[g] ..
+// offs[g+1]-1 of the permuted activations) and, when present, the shared expert
+// (T_shared rows).  Each group is cut into token tiles x feature tiles; a table
+// of cumulative tile counts, built in shared memory by every CTA from the expert
+// offsets, maps a global tile index back to its group.  Persistent CTAs take tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ...
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+
+#include "ffn.cuh"
+#include "tc.cuh"
+
+namespace moe {
+namespace grouped {
+
+constexpr int kMaxGroups = 2048 + 1;
+
+struct Params {
+  const int32_t *offs;  // [P + 1]
+  const int32_t *p2l;   // [P] or null
+  int P, N, T_shared, E_w;
+  int feat;             // output features: I (gate/up) or d (down)
+  int K;                // reduction length: d (gate/up) or I (down)
+  int w_rows;           // weight rows per expert: 2I (gate/up) or d (down)
+  int shared_row0;      // row of the shared group's first token in its token map
+  void *out;            // h or y
+  int64_t ld;           // elements per output row
+  int32_t *err;
+  // block-scaled e4m3 only
+  const float *a_scales;  // [rows, K/128] scales of the token operand
+  const float *w_scales;  // [E_w, w_rows/128, K/128]
+  float *out_scales;      // gate/up: [rows, I/128] scales of the quantised h
+};
+
+struct Tile {
+  int e, tok_row, out_row, valid, nt;
+  bool shared;
+};
+
+__device__ __forceinline__ void group_span(const Params &p, int g, int *r0, int *n) {
+  if (g < p.P) {
+    const int a = min(max(p.offs[g], 0), p.N);
+    const int b = min(max(p.offs[g + 1], 0), p.N);
+    *r0 = a;
+    *n = max(b - a, 0);
+  } else {
+    *r0 = 0;
+    *n = p.T_shared;
+  }
+}
+
+// In-place inclusive scan of a[0..n) by the whole block (blockDim.x <= 1024).
+__device__ __forceinline__ void block_scan(int *a, int n) {
+  __shared__ int wsum[32];
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+  int s = 0;
+  for (int i = lo; i < hi; ++i) s += a[i];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int v = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) wsum[warp] = v;
+  __syncthreads();
+  int off = v - s;
+  for (int w = 0; w < warp; ++w) off += wsum[w];
+  for (int i = lo; i < hi; ++i) {
+    off += a[i];
+    a[i] = off;
+  }
+  __syncthreads();
+}
+
+// tile_start[0..G]: cumulative tile counts per group.  Call with all threads.
+template <int kTokTile>
+__device__ __forceinline__ void build_tile_table(const Params &p, int *tile_start, int G, int NT) {
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    int r0, n;
+    group_span(p, g, &r0, &n);
+    tile_start[g + 1] = n > 0 ? ((n + kTokTile - 1) / kTokTile) * NT : 0;
+  }
+  if (threadIdx.x == 0) tile_start[0] = 0;
+  __syncthreads();
+  block_scan(tile_start + 1, G);
+}
+
+// kTokTile == 32 (swap): token tiles of one feature block run back to back.
+// Otherwise (wide): feature blocks of one token tile run back to back.
+template <int kTokTile>
+__device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, int G, int NT, int tile) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo, local = tile - tile_start[g];
+  int r0, n;
+  group_span(p, g, &r0, &n);
+  const int MT = (n + kTokTile - 1) / kTokTile;
+  int mt, nt;
+  if (kTokTile == 32) {
+    nt = local / MT;
+    mt = local % MT;
+  } else {
+    mt = local / NT;
+    nt = local % NT;
+  }
+  Tile t;
+  t.shared = g >= p.P;
+  int e = t.shared ? p.E_w - 1 : (p.p2l ? p.p2l[g] : g);
+  if (e < 0 || e >= p.E_w) e = -1;
+  t.e = e;
+  t.nt = nt;
+  t.valid = min(kTokTile, n - mt * kTokTile);
+  t.tok_row = (t.shared ? p.shared_row0 : r0) + mt * kTokTile;
+  t.out_row = (t.shared ? p.N : r0) + mt * kTokTile;
+  return t;
+}
+
+// ------------------------------------------------------------------ host side
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements; boxes of
+// box_rows x (128 / esize) elements (128 bytes), 128-byte swizzle, zero fill outside.
+inline bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, int esize, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0 || !aligned(base, 16) || (cols * esize) % 16) return false;
+  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esize), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+// Tile orientation: "swap" for few rows per expert, "wide" otherwise; the
+// environment variable MOE_B300_FFN_TILES=swap|wide overrides the choice.
+inline bool use_swap(int64_t N, int64_t P) {
+  const char *env = std::getenv("MOE_B300_FFN_TILES");
+  if (env && !std::strcmp(env, "swap")) return true;
+  if (env && !std::strcmp(env, "wide")) return false;
+  return N < 64 * P;
+}
+
+inline Params base_params(const FfnArgs &f) {
+  Params p{};
+  p.offs = f.offs;
+  p.p2l = f.p2l;
+  p.P = (int)f.P;
+  p.N = (int)f.N;
+  p.T_shared = (int)f.T_shared;
+  p.E_w = (int)f.w->E_w;
+  p.err = f.err;
+  return p;
+}
+
+}  // namespace grouped
+}  // namespace moe

@@ -294,8 +294,8 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
   if (chunks > 0) {
     const size_t smem = (size_t)kCountWarps * P * 4;
     if (smem > 48 * 1024) {
-      if (cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
+      if (cuda_status(cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          MOE_OK)
         return MOE_ERR_CUDA;
     }
     layout_count_kernel<<<chunks, 256, smem, st>>>(topk_ids, N, (int)P, m, hist, chunk_rank, err);

@@ -49,7 +49,7 @@ moe_status_t scratch_on_current_device(void **out) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    if (cuda_status(cudaGetSymbolAddress(&p, g_layout_scratch)) != MOE_OK || !p) return MOE_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

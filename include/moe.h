@@ -134,6 +134,10 @@ typedef struct {
 /* Static text for a status code. */
 const char *moe_status_string(moe_status_t s);
 
+/* Text of the last CUDA error behind a MOE_ERR_CUDA returned to the calling
+ * thread ("" when there was none).  The pages have no counterpart; diagnostics. */
+const char *moe_last_cuda_error(void);
+
 /* Route ("6.4 ...", section 3.1, step 1 "Route": top-k experts and weights per
  * token).  logits [T, E] fp32.  Experts are chosen by (logit descending, index
  * ascending); -0 and +0 tie.  topk_ids [T, k] int32 in that order; topk_w [T, k]

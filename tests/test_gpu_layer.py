@@ -118,3 +118,12 @@ def test_layer_prefill_bf16_skew():
 
 def test_layer_prefill_bf16_skew_eplb():
     check(mi.config(3), sample=sample_tokens(8192, n=3, seed=1))
+
+
+# ------------------------------------------------------------------ fp8 workload
+def test_layer_fp8_small_full():
+    check(mi.config(4).scaled(T=200, d=256, E=16, I=256, R=4))
+
+
+def test_layer_prefill_fp8_skew():
+    check(mi.config(4), sample=sample_tokens(16384, n=3, seed=2))
