@@ -369,13 +369,28 @@ def run_ours(args, world, rank, local):
 
 
 # ------------------------------------------------------------------ the oracle, timed
+def _affinity_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
 def oracle_threads():
+    """Threads numpy's BLAS runs the oracle's matmuls with.  Without threadpoolctl
+    this is OpenBLAS's default: OPENBLAS_NUM_THREADS / OMP_NUM_THREADS, else every
+    core the process may run on."""
     try:
         from threadpoolctl import threadpool_info
         n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
-        return max(n) if n else 1
+        if n:
+            return max(n)
     except Exception:
-        return 1
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return _affinity_cores()
 
 
 class host_cores:
@@ -387,7 +402,7 @@ class host_cores:
         self.ctx = None
         try:
             from threadpoolctl import threadpool_limits
-            self.ctx = threadpool_limits(limits=os.cpu_count() or 1, user_api="blas")
+            self.ctx = threadpool_limits(limits=_affinity_cores(), user_api="blas")
         except Exception:
             pass
         return self

@@ -56,4 +56,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// silu for the tensor-core epilogues, whose results are rounded to bf16 or e4m3:
+// the fast exponential and a reciprocal (z -> -inf gives z * 0 = -0).
+__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
 }  // namespace moe

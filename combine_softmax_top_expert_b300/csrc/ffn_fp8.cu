@@ -189,39 +189,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
       bool ok = true;
+      // scales of the next K block are loaded one block ahead
+      float xs_n = row_ok ? __ldg(sa) : 0.f, s0_n = __ldg(sw0), s1_n = kGated ? __ldg(sw1) : 0.f;
+      // gated: gate columns [64*half, +64) and up columns [128 + 64*half, +64)
+      // down:  columns [128*half, +128)
+      const uint32_t c0 = kGated ? 64 * half : 128 * half;
+      const uint32_t c1 = kGated ? 128 + 64 * half : 128 * half + 64;
       for (int kb = 0; kb < KB; ++kb, ++gk) {
         const int b = gk & 1;
-        const float xs = row_ok ? __ldg(sa + kb) : 0.f;
-        const float f0 = xs * __ldg(sw0 + kb);
-        const float f1 = kGated ? xs * __ldg(sw1 + kb) : f0;
+        const float f0 = xs_n * s0_n;
+        const float f1 = kGated ? xs_n * s1_n : f0;
+        if (kb + 1 < KB) {
+          xs_n = row_ok ? __ldg(sa + kb + 1) : 0.f;
+          s0_n = __ldg(sw0 + kb + 1);
+          if (kGated) s1_n = __ldg(sw1 + kb + 1);
+        }
         if (!mbar_wait(dfull(b), (gk >> 1) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         fence_after();
         const uint32_t d = lane_base + b * kAccCols;
-        // gated: gate columns [64*half, +64) and up columns [128 + 64*half, +64)
-        // down:  columns [128*half, +128)
-        const uint32_t c0 = kGated ? 64 * half : 128 * half;
-        const uint32_t c1 = kGated ? 128 + 64 * half : 128 * half + 64;
+        float v[64];
+        tmem_ld32(d + c0, v);
+        tmem_ld32(d + c0 + 32, v + 32);
+        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float v[32];
-          tmem_ld32(d + c0 + 32 * j, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc0[32 * j + i] = fmaf(v[i], f0, acc0[32 * j + i]);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float v[32];
-          tmem_ld32(d + c1 + 32 * j, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc1[32 * j + i] = fmaf(v[i], f1, acc1[32 * j + i]);
-        }
+        for (int i = 0; i < 64; ++i) acc0[i] = fmaf(v[i], f0, acc0[i]);
+        tmem_ld32(d + c1, v);
+        tmem_ld32(d + c1 + 32, v + 32);
+        tmem_wait_ld();
         fence_before();
-        mbar_arrive(dempty(b));
+        mbar_arrive(dempty(b));  // the accumulator is in registers: let the next K block in
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc1[i] = fmaf(v[i], f1, acc1[i]);
       }
       if (!ok) break;
       if (t.e < 0 && r == 0 && half == 0) raise_dev(p.err, MOE_DEV_LAYOUT);
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          acc0[i] = silu(acc0[i]) * acc1[i];
+          acc0[i] = silu_fast(acc0[i]) * acc1[i];
           amax = fmaxf(amax, fabsf(acc0[i]));
         }
         // the row's two halves meet through shared memory; the slot alternates by tile
@@ -240,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(xbar, it & 1, abort_flag, p.err)) break;
         amax = fmaxf(slot[r], slot[128 + r]);
         const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        // h is an intermediate: multiplying by 1/scale instead of dividing moves the
+        // value before rounding by at most an fp32 ulp
+        const float inv = __frcp_rn(scale);
         if (row_ok) {
           uint8_t *orow = static_cast<uint8_t *>(p.out) + (int64_t)grow * p.ld + t.nt * 128 + 64 * half;
 #pragma unroll
@@ -248,8 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int j = 16 * c + 4 * i;
-              w[i] = e4m3x2(__fdiv_rn(acc0[j], scale), __fdiv_rn(acc0[j + 1], scale)) |
-                     (e4m3x2(__fdiv_rn(acc0[j + 2], scale), __fdiv_rn(acc0[j + 3], scale)) << 16);
+              w[i] = e4m3x2(acc0[j] * inv, acc0[j + 1] * inv) | (e4m3x2(acc0[j + 2] * inv, acc0[j + 3] * inv) << 16);
             }
             reinterpret_cast<uint4 *>(orow)[c] = make_uint4(w[0], w[1], w[2], w[3]);
           }

@@ -48,21 +48,35 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try, but a thread whose phase is not complete sleeps until it completes
+// or `hint_ns` has passed, instead of returning at once: waiting warps then leave
+// the issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when the
 // CTA's abort flag is set or after kTimeoutNs, in which case it sets the flag
-// and reports MOE_DEV_TIMEOUT.
+// and reports MOE_DEV_TIMEOUT.  Each sleep lasts at most 0.5 ms, so the flag and
+// the clock are looked at between sleeps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
-        *abort_flag = 1;
-        raise_dev(err, MOE_DEV_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_sleep(bar, parity, 500000u)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      raise_dev(err, MOE_DEV_TIMEOUT);
+      return false;
     }
   }
 }
@@ -140,7 +154,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane
 // (warp's lane quarter) + i, columns col .. col+31.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
