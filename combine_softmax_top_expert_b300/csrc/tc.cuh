@@ -65,10 +65,13 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, ui
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when the
 // CTA's abort flag is set or after kTimeoutNs, in which case it sets the flag
-// and reports MOE_DEV_TIMEOUT.  Each sleep lasts at most 0.5 ms, so the flag and
-// the clock are looked at between sleeps.
+// and reports MOE_DEV_TIMEOUT.  Short waits poll (the fastest wake-up); after a
+// while the thread sleeps at most 0.5 ms at a time, looking at the flag and the
+// clock between sleeps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
-  if (mbar_try(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try_sleep(bar, parity, 500000u)) return true;
