@@ -48,8 +48,7 @@ static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_e4m3(const Params p, const __grid_constant__ CUtensorMap tm_tok,
-                      const __grid_constant__ CUtensorMap tm_w) {
+    grouped_gemm_e4m3(const Params p, const __grid_constant__ CUtensorMap tm_tok) {
   constexpr int kFeatTile = kGated ? 128 : 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -87,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 32) {
     tma_prefetch(&tm_tok);
-    tma_prefetch(&tm_w);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), 512);
@@ -109,7 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = grouped::decode<128>(p, tile_start, G, NT, tile);
-      const int wrow = max(t.e, 0) * p.w_rows + t.nt * kFeatTile;
+      const int e = max(t.e, 0);
+      // gated: the gate+up block of this 128-feature block; down: the two tiles of
+      // these 256 output features
+      const int rt0 = kGated ? t.nt : 2 * t.nt;
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
@@ -118,13 +119,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = stage0 + s * kStage, bar = full(s);
         mbar_expect_tx(bar, kStage);
-        const int kx = kb * 128;
-        tma_load_2d(st, &tm_tok, bar, kx, t.tok_row);
+        tma_load_2d(st, &tm_tok, bar, kb * 128, t.tok_row);
         if (kGated) {
-          tma_load_2d(st + kABytes, &tm_w, bar, kx, wrow);
-          tma_load_2d(st + kABytes + 16384, &tm_w, bar, kx, wrow + p.feat);
+          bulk_load(st + kABytes, grouped::weight_block(p, e, rt0, kb, KB, grouped::kPairBytes), grouped::kPairBytes,
+                    bar);
         } else {
-          tma_load_2d(st + kABytes, &tm_w, bar, kx, wrow);
+          bulk_load(st + kABytes, grouped::weight_block(p, e, rt0, kb, KB, grouped::kTileBytes), grouped::kTileBytes,
+                    bar);
+          bulk_load(st + kABytes + grouped::kTileBytes, grouped::weight_block(p, e, rt0 + 1, kb, KB, grouped::kTileBytes),
+                    grouped::kTileBytes, bar);
         }
         ++issued;
         if (++s == kStages) {
@@ -293,13 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kGated>
-moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, cudaStream_t st) {
+moe_status_t launch(const Params &p, const CUtensorMap &a, cudaStream_t st) {
   auto k = grouped_gemm_e4m3<kGated>;
   if (cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem)) != MOE_OK)
     return MOE_ERR_CUDA;
   const int grid = grouped::sm_count();
   if (grid <= 0) return MOE_ERR_CUDA;
-  k<<<grid, kThreads, kSmem, st>>>(p, a, b);
+  k<<<grid, kThreads, kSmem, st>>>(p, a);
   return launch_status();
 }
 
@@ -319,19 +322,21 @@ moe_status_t gate_up_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (f.N == 0) return MOE_OK;
   if (!f.x_scales || !f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
-  CUtensorMap m_x, m_w13;
+  CUtensorMap m_x;
   if (!grouped::make_map(&m_x, f.x_perm, f.N, w.d, 1, 128)) return MOE_ERR_INVALID_ARG;
-  if (!grouped::make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * w.I, w.d, 1, 128)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)w.I;
   p.K = (int)w.d;
   p.w_rows = (int)(2 * w.I);
+  p.w = static_cast<const uint8_t *>(w.w13);
+  p.w_tiles = (int)(w.I / 128);  // gate+up blocks of 128 features
   p.out = f.h;
   p.ld = w.I;
   p.a_scales = f.x_scales;
   p.w_scales = w.s13;
   p.out_scales = f.h_scales;
-  return launch<true>(p, m_x, m_w13, st);
+  return launch<true>(p, m_x, st);
 }
 
 moe_status_t down_e4m3(const FfnArgs &f, cudaStream_t st) {
@@ -340,18 +345,20 @@ moe_status_t down_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (f.N == 0) return MOE_OK;
   if (!f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
-  CUtensorMap m_h, m_w2;
+  CUtensorMap m_h;
   if (!grouped::make_map(&m_h, f.h, f.N, w.I, 1, 128)) return MOE_ERR_INVALID_ARG;
-  if (!grouped::make_map(&m_w2, w.w2, (uint64_t)w.E_w * w.d, w.I, 1, 256)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)w.d;
   p.K = (int)w.I;
   p.w_rows = (int)w.d;
+  p.w = static_cast<const uint8_t *>(w.w2);
+  p.w_tiles = (int)(w.d / 128);
   p.out = f.y;
   p.ld = w.d;
   p.a_scales = f.h_scales;
   p.w_scales = w.s2;
-  return launch<false>(p, m_h, m_w2, st);
+  return launch<false>(p, m_h, st);
 }
 
 }  // namespace moe

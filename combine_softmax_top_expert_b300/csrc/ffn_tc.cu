@@ -49,7 +49,7 @@ struct Cfg {
 template <bool kGated, bool kSwap, int kBW>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16(const Params p, const __grid_constant__ CUtensorMap tm_tok,
-                      const __grid_constant__ CUtensorMap tm_sh, const __grid_constant__ CUtensorMap tm_w) {
+                      const __grid_constant__ CUtensorMap tm_sh) {
   using C = Cfg<kGated, kSwap, kBW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -85,7 +85,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     tma_prefetch(&tm_tok);
     tma_prefetch(&tm_sh);
-    tma_prefetch(&tm_w);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&misc[0]), C::kTmemCols);
@@ -108,7 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap *tmt = (kGated && t.shared) ? &tm_sh : &tm_tok;
       const int nb = kSwap ? (t.valid + 15) / 16 : 0;
       const uint32_t bytes = C::kABytes + (kSwap ? nb * 2048 : C::kBBytes);
-      const int wrow = max(t.e, 0) * p.w_rows + t.nt * C::kFeatTile;
+      const int e = max(t.e, 0);
+      // gated: the gate+up block of this 128-feature block; down: the tile(s) of
+      // this block of output features
+      const int rt0 = kGated ? t.nt : t.nt * (C::kFeatTile / 128);
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
@@ -118,14 +120,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = stage0 + s * C::kStage, bar = full(s);
         mbar_expect_tx(bar, bytes);
         const int kx = kb * 64;
+        const uint32_t wdst = kSwap ? st : st + C::kABytes;
+        auto wload = [&](uint32_t dst, const uint8_t *src, uint32_t n) { bulk_load(dst, src, n, bar); };
+        if (kGated) {
+          wload(wdst, grouped::weight_block(p, e, rt0, kb, KB, grouped::kPairBytes), grouped::kPairBytes);
+        } else {
+          wload(wdst, grouped::weight_block(p, e, rt0, kb, KB, grouped::kTileBytes), grouped::kTileBytes);
+          if (!kSwap && kBW == 256)
+            wload(wdst + grouped::kTileBytes, grouped::weight_block(p, e, rt0 + 1, kb, KB, grouped::kTileBytes),
+                  grouped::kTileBytes);
+        }
         if (kSwap) {
-          tma_load_2d(st, &tm_w, bar, kx, wrow);
-          if (kGated) tma_load_2d(st + 16384, &tm_w, bar, kx, wrow + p.feat);
           for (int i = 0; i < nb; ++i) tma_load_2d(st + C::kABytes + i * 2048, tmt, bar, kx, t.tok_row + 16 * i);
         } else {
           tma_load_2d(st, tmt, bar, kx, t.tok_row);
-          tma_load_2d(st + C::kABytes, &tm_w, bar, kx, wrow);
-          if (kGated) tma_load_2d(st + C::kABytes + 16384, &tm_w, bar, kx, wrow + p.feat);
         }
         ++issued;
         if (++s == C::kStages) {
@@ -246,15 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kGated, bool kSwap, int kBW>
-moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
-                    cudaStream_t st) {
+moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, cudaStream_t st) {
   using Cf = Cfg<kGated, kSwap, kBW>;
   auto k = grouped_gemm_bf16<kGated, kSwap, kBW>;
   if (cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem)) != MOE_OK)
     return MOE_ERR_CUDA;
   const int grid = grouped::sm_count();
   if (grid <= 0) return MOE_ERR_CUDA;
-  k<<<grid, kThreads, Cf::kSmem, st>>>(p, a, b, c);
+  k<<<grid, kThreads, Cf::kSmem, st>>>(p, a, b);
   return launch_status();
 }
 
@@ -275,7 +282,7 @@ moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
   if (f.N + f.T_shared == 0) return MOE_OK;
   const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
   const uint32_t tok_box = swap ? 16 : 128;
-  CUtensorMap m_x, m_sh, m_w13;
+  CUtensorMap m_x, m_sh;
   const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
   const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
   if (!grouped::make_map(&m_x, xsrc, xrows, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
@@ -284,15 +291,17 @@ moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
   } else {
     m_sh = m_x;
   }
-  if (!grouped::make_map(&m_w13, w.w13, (uint64_t)w.E_w * 2 * I, d, 2, 128)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)I;
   p.K = (int)d;
   p.w_rows = (int)(2 * I);
+  p.w = static_cast<const uint8_t *>(w.w13);
+  p.w_tiles = (int)(I / 128);  // gate+up blocks of 128 features
   p.shared_row0 = 0;
   p.out = f.h;
   p.ld = I;
-  return swap ? launch<true, true, 128>(p, m_x, m_sh, m_w13, st) : launch<true, false, 128>(p, m_x, m_sh, m_w13, st);
+  return swap ? launch<true, true, 128>(p, m_x, m_sh, st) : launch<true, false, 128>(p, m_x, m_sh, st);
 }
 
 moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
@@ -303,18 +312,20 @@ moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
   if (rows == 0) return MOE_OK;
   const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
   const int kbw = (d % 256 == 0) ? 256 : 128;
-  CUtensorMap m_h, m_w2;
+  CUtensorMap m_h;
   if (!grouped::make_map(&m_h, f.h, rows, I, 2, swap ? 16 : 128)) return MOE_ERR_INVALID_ARG;
-  if (!grouped::make_map(&m_w2, w.w2, (uint64_t)w.E_w * d, I, 2, swap ? 128 : kbw)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)d;
   p.K = (int)I;
   p.w_rows = (int)d;
+  p.w = static_cast<const uint8_t *>(w.w2);
+  p.w_tiles = (int)(d / 128);
   p.shared_row0 = (int)f.N;
   p.out = f.y;
   p.ld = d;
-  if (swap) return launch<false, true, 128>(p, m_h, m_h, m_w2, st);
-  return kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, m_w2, st) : launch<false, false, 128>(p, m_h, m_h, m_w2, st);
+  if (swap) return launch<false, true, 128>(p, m_h, m_h, st);
+  return kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, st) : launch<false, false, 128>(p, m_h, m_h, st);
 }
 
 }  // namespace moe

@@ -32,6 +32,9 @@ struct Params {
   void *out;            // h or y
   int64_t ld;           // elements per output row
   int32_t *err;
+  // packed weights (see weight_block)
+  const uint8_t *w;
+  int w_tiles;            // tiles per expert
   // block-scaled e4m3 only
   const float *a_scales;  // [rows, K/128] scales of the token operand
   const float *w_scales;  // [E_w, w_rows/128, K/128]
@@ -42,6 +45,20 @@ struct Tile {
   int e, tok_row, out_row, valid, nt;
   bool shared;
 };
+
+// The packed weights are tiled: for expert e, tile t and K block kb (128 bytes
+// of every row), one contiguous block whose rows are 128 bytes apart with the
+// 16-byte chunks of row r permuted by chunk ^ (r % 8) -- the arrangement the
+// 128-byte swizzle gives in shared memory -- so one bulk copy moves it straight
+// into MMA operand tiles.  W_down^T: 128-row tiles (16 KB blocks).  W_gate^T and
+// W_up^T: 256-row tiles holding the gate rows then the up rows of the same 128
+// features (32 KB blocks).
+constexpr int kTileBytes = 128 * 128;
+constexpr int kPairBytes = 2 * kTileBytes;
+
+__device__ __forceinline__ const uint8_t *weight_block(const Params &p, int e, int t, int kb, int KB, int bytes) {
+  return p.w + (((int64_t)e * p.w_tiles + t) * KB + kb) * bytes;
+}
 
 __device__ __forceinline__ void group_span(const Params &p, int g, int *r0, int *n) {
   if (g < p.P) {

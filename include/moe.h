@@ -88,8 +88,16 @@ typedef struct {
 
 /* Packed expert weights (produced by moe_pack_weights), one set per logical
  * expert; with has_shared the set at index E is the always-on shared expert.
- *   w13: [E_w, 2I, d]  rows 0..I-1 = W_gate^T, rows I..2I-1 = W_up^T (d contiguous)
- *   w2 : [E_w, d, I]   W_down^T (I contiguous)
+ *   w13: [E_w, 2I, d]  rows 0..I-1 = W_gate^T, rows I..2I-1 = W_up^T (d per row)
+ *   w2 : [E_w, d, I]   W_down^T (I per row)
+ *   MOE_F32 rows are stored plainly.  MOE_BF16 and MOE_E4M3 rows are tiled: per
+ *   expert, tiles cut into 128-byte column blocks (tile major, then column
+ *   block); inside a block the rows are 128 bytes apart and the 16-byte chunk j
+ *   of block row r sits at chunk j ^ (r % 8), the arrangement the tensor cores
+ *   read from shared memory, so each block is one contiguous copy.  w2 tiles are
+ *   128 rows (16 KB blocks); w13 tiles are 256 rows: the W_gate^T rows, then the
+ *   W_up^T rows, of the same 128 features (32 KB blocks).
+ *   (Requires d % 128 == 0 and I % 128 == 0; base pointers 16-byte aligned.)
  *   e4m3 only: s13 [E_w, 2I/128, d/128], s2 [E_w, d/128, I/128] fp32 block scales,
  *   dequantised weight = code * scale of its 128x128 block. */
 typedef struct {
@@ -289,8 +297,8 @@ moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_dt,
 
 /* One-time weight packing for one expert (not part of the timed forward).
  * Logical w_gate [d, I], w_up [d, I], w_down [I, d] in src_dt (MOE_F32 or
- * MOE_BF16) -> w13_e [2I, d] and w2_e [d, I] in dst_dt (the transposes, see
- * moe_weights_t).  dst_dt = MOE_E4M3 (from bf16 or f32) quantises per 128x128
+ * MOE_BF16) -> w13_e [2I, d] and w2_e [d, I] in dst_dt (the transposes, tiled
+ * for bf16 and e4m3 as moe_weights_t describes).  dst_dt = MOE_E4M3 (from bf16 or f32) quantises per 128x128
  * block of the logical matrices with the moe_permute rule and writes the block
  * scales s13_e [2I/128, d/128] and s2_e [d/128, I/128]. */
 moe_status_t moe_pack_weights(const void *w_gate, const void *w_up,

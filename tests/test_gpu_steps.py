@@ -253,6 +253,34 @@ def test_combine_and_identity_experts(ci, T):
 
 
 # ------------------------------------------------------------------ weight packing
+def tiled(m, rows_per_tile=128):
+    """The packed layout of a K-major matrix m [rows, K] (uint16 or uint8):
+    rows_per_tile x 128-byte blocks, tile major then column block, the 16-byte
+    chunk j of block row r moved to j ^ (r % 8)."""
+    b = np.ascontiguousarray(m).view(np.uint8)
+    rows, nb = b.shape
+    t = b.reshape(rows // rows_per_tile, rows_per_tile, nb // 128, 8, 16)
+    out = np.empty_like(t)
+    for r in range(rows_per_tile):
+        for j in range(8):
+            out[:, r, :, j ^ (r % 8), :] = t[:, r, :, j, :]
+    return out.transpose(0, 2, 1, 3, 4).reshape(-1)
+
+
+def gate_up_interleaved(g_t, u_t):
+    """W_gate^T and W_up^T rows in 256-row tiles: the gate rows then the up rows of
+    each group of 128 features."""
+    I = g_t.shape[0]
+    parts = []
+    for f in range(0, I, 128):
+        parts += [g_t[f:f + 128], u_t[f:f + 128]]
+    return np.concatenate(parts)
+
+
+def packed_bytes(t):
+    return t.contiguous().view(torch.uint8).cpu().numpy().reshape(-1)
+
+
 @pytest.mark.parametrize("dst", ["bf16", "fp8", "fp32"])
 def test_pack_weights(dst):
     d, I = 256, 384
@@ -267,12 +295,12 @@ def test_pack_weights(dst):
         assert np.array_equal(pw.w13[1].cpu().numpy(), np.concatenate([wg.T, wu.T]))
         assert np.array_equal(pw.w2[1].cpu().numpy(), wd.T)
     elif dst == "bf16":
-        assert np.array_equal(host_bf16_bits(pw.w13[1]), np.concatenate([wg.T, wu.T]))
-        assert np.array_equal(host_bf16_bits(pw.w2[1]), wd.T)
+        assert np.array_equal(packed_bytes(pw.w13[1]), tiled(gate_up_interleaved(wg.T, wu.T), 256))
+        assert np.array_equal(packed_bytes(pw.w2[1]), tiled(wd.T))
     else:
         f = [mi.f32_from_bf16_bits(a) for a in (wg, wu, wd)]
         qs = [O.quantize_blocks(a) for a in f]
-        assert np.array_equal(pw.w13[1].cpu().numpy(), np.concatenate([qs[0][0].T, qs[1][0].T]))
-        assert np.array_equal(pw.w2[1].cpu().numpy(), qs[2][0].T)
+        assert np.array_equal(packed_bytes(pw.w13[1]), tiled(gate_up_interleaved(qs[0][0].T, qs[1][0].T), 256))
+        assert np.array_equal(packed_bytes(pw.w2[1]), tiled(qs[2][0].T))
         assert np.array_equal(pw.s13[1].cpu().numpy(), np.concatenate([qs[0][1].T, qs[1][1].T]))
         assert np.array_equal(pw.s2[1].cpu().numpy(), qs[2][1].T)
