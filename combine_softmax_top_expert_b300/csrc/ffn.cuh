@@ -36,7 +36,11 @@ moe_status_t gate_up_f32(const FfnArgs &a, cudaStream_t st);
 moe_status_t down_f32(const FfnArgs &a, cudaStream_t st);
 moe_status_t gate_up_bf16(const FfnArgs &a, cudaStream_t st);
 moe_status_t down_bf16(const FfnArgs &a, cudaStream_t st);
+moe_status_t gate_up_bf16_pair(const FfnArgs &a, cudaStream_t st);
+moe_status_t down_bf16_pair(const FfnArgs &a, cudaStream_t st);
 moe_status_t gate_up_e4m3(const FfnArgs &a, cudaStream_t st);
 moe_status_t down_e4m3(const FfnArgs &a, cudaStream_t st);
+moe_status_t gate_up_e4m3_pair(const FfnArgs &a, cudaStream_t st);
+moe_status_t down_e4m3_pair(const FfnArgs &a, cudaStream_t st);
 
 }  // namespace moe

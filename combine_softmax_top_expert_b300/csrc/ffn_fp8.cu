@@ -10,7 +10,8 @@
 // Two TMEM accumulators alternate so the tensor cores work on block kb+1 while the
 // epilogue folds block kb.
 //
-// Tiles are "wide": A = 128 token rows, B = 256 weight rows (gate 128 + up 128 of
+// This is the one-SM form, for few rows per expert; ffn_fp8_pair.cu holds the
+// SM-pair form used for many.  Tiles: A = 128 token rows, B = 256 weight rows (gate 128 + up 128 of
 // one 128-feature block, or 256 output features of W_down), K blocks of 128 bytes.
 // 12 warps: warp 0 TMA, warp 1 MMA, warps 4-11 epilogue; epilogue warps w and w+4
 // share TMEM lanes (token rows) and split the 256 columns.
@@ -322,6 +323,9 @@ moe_status_t gate_up_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (f.N == 0) return MOE_OK;
   if (!f.x_scales || !f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
+  if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
+  // the one-SM tiles stay the default: the pair form loses more to the promotion chain
+  if (grouped::tile_kind(f.N, f.P, grouped::Tiles::kWide) == grouped::Tiles::kPair) return gate_up_e4m3_pair(f, st);
   CUtensorMap m_x;
   if (!grouped::make_map(&m_x, f.x_perm, f.N, w.d, 1, 128)) return MOE_ERR_INVALID_ARG;
   if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
@@ -345,6 +349,9 @@ moe_status_t down_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (f.N == 0) return MOE_OK;
   if (!f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
+  if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;
+  // the one-SM tiles stay the default: the pair form loses more to the promotion chain
+  if (grouped::tile_kind(f.N, f.P, grouped::Tiles::kWide) == grouped::Tiles::kPair) return down_e4m3_pair(f, st);
   CUtensorMap m_h;
   if (!grouped::make_map(&m_h, f.h, f.N, w.I, 1, 128)) return MOE_ERR_INVALID_ARG;
   if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;

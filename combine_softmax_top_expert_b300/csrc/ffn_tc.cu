@@ -13,7 +13,8 @@
 //
 // Tile orientations (both K-major operands, 128-byte swizzled, K blocks of 64):
 //   wide  A = 128 token rows, B = weight rows (gate 128 + up 128, or 256 of
-//         W_down): one 128x256xK tile per feature block.  For many rows per expert.
+//         W_down): one 128x256xK tile per feature block.  The one-SM form of the
+//         pair tiles (ffn_pair.cu) used for many rows per expert.
 //   swap  A = 128 weight rows (gate and up as two MMAs), B = up to 32 token rows:
 //         D is features x tokens, so a group of a few tokens streams its weights
 //         at HBM speed without padding tokens to 128.  For decode-sized batches.
@@ -280,7 +281,9 @@ moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I;
   if (f.N + f.T_shared == 0) return MOE_OK;
-  const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
+  const grouped::Tiles kind = grouped::tile_kind(f.N + f.T_shared, f.P);
+  if (kind == grouped::Tiles::kPair) return gate_up_bf16_pair(f, st);
+  const bool swap = kind == grouped::Tiles::kSwap;
   const uint32_t tok_box = swap ? 16 : 128;
   CUtensorMap m_x, m_sh;
   const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
@@ -310,8 +313,10 @@ moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
   if (rows == 0) return MOE_OK;
-  const bool swap = grouped::use_swap(f.N + f.T_shared, f.P);
+  const grouped::Tiles kind = grouped::tile_kind(rows, f.P);
   const int kbw = (d % 256 == 0) ? 256 : 128;
+  if (kind == grouped::Tiles::kPair && kbw == 256) return down_bf16_pair(f, st);
+  const bool swap = kind == grouped::Tiles::kSwap;
   CUtensorMap m_h;
   if (!grouped::make_map(&m_h, f.h, rows, I, 2, swap ? 16 : 128)) return MOE_ERR_INVALID_ARG;
   if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;

@@ -12,6 +12,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <utility>
 
 #include "ffn.cuh"
 #include "tc.cuh"
@@ -173,6 +174,21 @@ inline bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
          CUDA_SUCCESS;
 }
 
+// 2-D map over packed (tiled, already swizzled) weights seen as `rows` rows of 128
+// bytes; boxes of box_rows rows copied as they are (no swizzle).  Row
+// ((e * w_tiles + t) * KB + kb) * tile_rows + i is row i of weight_block(e, t, kb).
+inline bool make_map_tiled(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0 || rows > (1ull << 31) || !aligned(base, 16)) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -181,13 +197,49 @@ inline int sm_count() {
   return n;
 }
 
-// Tile orientation: "swap" for few rows per expert, "wide" otherwise; the
-// environment variable MOE_B300_FFN_TILES=swap|wide overrides the choice.
-inline bool use_swap(int64_t N, int64_t P) {
+// Launch `kernel` as clusters of two CTAs (the SM-pair tiles), as many pairs as
+// the GPU holds at once with `threads` threads and `smem` bytes of dynamic shared
+// memory per CTA; *pairs caches that count between calls.
+template <typename... KArgs, typename... Args>
+moe_status_t launch_pairs(void (*kernel)(KArgs...), int threads, size_t smem, int *pairs, cudaStream_t st,
+                          Args &&...args) {
+  if (cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != MOE_OK)
+    return MOE_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (*pairs <= 0) {
+    const int sms = sm_count();
+    cfg.gridDim = dim3(2 * (sms > 1 ? sms / 2 : 1));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    *pairs = n;
+  }
+  cfg.gridDim = dim3(2 * *pairs);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+}
+
+// Tile orientation: "swap" for few rows per expert, "pair" (two SMs per tile)
+// otherwise; "wide" is the one-SM form of pair.  The environment variable
+// MOE_B300_FFN_TILES=swap|wide|pair overrides the choice.
+enum class Tiles { kSwap, kWide, kPair };
+inline Tiles tile_kind(int64_t N, int64_t P, Tiles many_rows = Tiles::kPair) {
   const char *env = std::getenv("MOE_B300_FFN_TILES");
-  if (env && !std::strcmp(env, "swap")) return true;
-  if (env && !std::strcmp(env, "wide")) return false;
-  return N < 64 * P;
+  if (env && !std::strcmp(env, "swap")) return Tiles::kSwap;
+  if (env && !std::strcmp(env, "wide")) return Tiles::kWide;
+  if (env && !std::strcmp(env, "pair")) return Tiles::kPair;
+  return N < 64 * P ? Tiles::kSwap : many_rows;
 }
 
 inline Params base_params(const FfnArgs &f) {

@@ -1,5 +1,5 @@
 """Grouped SwiGLU expert FFN (moe_expert_ffn) against the oracle, every output row,
-in both tile orientations of the tensor-core kernels."""
+in every tile orientation of the tensor-core kernels (swap, wide, SM pair)."""
 import os
 
 import numpy as np
@@ -71,18 +71,19 @@ def run_ffn(cfg, mode, logits=None, eplb=False):
 SMALL = mi.config(2).scaled(T=100, d=256, E=8, I=256, R=4, shared=False, zipf_bias=False)
 
 
-@pytest.mark.parametrize("mode", ["swap", "wide"])
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
 def test_ffn_small(mode):
     run_ffn(SMALL, mode)
 
 
-@pytest.mark.parametrize("mode", ["swap", "wide"])
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
 def test_ffn_shared_and_ragged(mode):
     # d = 384 is not a multiple of 256: the wide down GEMM takes 128-feature tiles
+    # and the pair down GEMM hands over to it
     run_ffn(SMALL.scaled(T=75, d=384, shared=True), mode)
 
 
-@pytest.mark.parametrize("mode", ["swap", "wide"])
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
 def test_ffn_skewed_groups(mode):
     # one expert gets almost every token: a group of many tiles with a ragged tail,
     # plus empty experts and single-row experts
@@ -94,7 +95,7 @@ def test_ffn_skewed_groups(mode):
     run_ffn(cfg, mode, logits=l)
 
 
-@pytest.mark.parametrize("mode", ["swap", "wide"])
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
 def test_ffn_eplb_aliases_weights(mode):
     cfg = SMALL.scaled(T=64, E=8, k=2, R=4, n_redundant=4, zipf_bias=True)
     run_ffn(cfg, mode, eplb=True)
@@ -103,3 +104,17 @@ def test_ffn_eplb_aliases_weights(mode):
 def test_ffn_single_token():
     run_ffn(SMALL.scaled(T=1), "swap")
     run_ffn(SMALL.scaled(T=1), "wide")
+    run_ffn(SMALL.scaled(T=1), "pair")
+
+
+def test_ffn_pair_tile_edges():
+    # three feature tiles per expert and groups from empty to several 256-row pair
+    # tiles, so the odd SM's half of a tile is full, partly filled or empty
+    cfg = SMALL.scaled(T=700, d=512, E=8, k=2, I=384, R=4)
+    rng = np.random.default_rng(1)
+    l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
+    l[:, 1] += 3.0
+    l[:, 6] -= 20.0
+    lay = run_ffn(cfg, "pair", logits=l)
+    counts = np.diff(lay["phys_offsets"])
+    assert counts.max() > 512 and (counts == 0).any()

@@ -2,6 +2,8 @@
 activations e4m3 per row per 128 channels) and the fp8 layer against the oracle.
 The tolerance is rms(gpu - oracle) <= 5e-2 * rms(oracle), checked over all outputs
 and also row by row so that one wrong scale block cannot hide in the average."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -32,7 +34,7 @@ def check_rms(got, ref, per_row=True):
     return err / rms(ref)
 
 
-def run_ffn_fp8(cfg, logits=None):
+def run_ffn_fp8(cfg, logits=None, mode=None):
     logits = mi.make_logits(cfg) if logits is None else logits
     ids, _ = O.route(logits, cfg.k)
     lay = O.dispatch_layout(ids, cfg.E, cfg.R)
@@ -49,8 +51,13 @@ def run_ffn_fp8(cfg, logits=None):
     offs = torch.from_numpy(lay["phys_offsets"].astype(np.int32)).cuda()
     xq_d = torch.from_numpy(np.ascontiguousarray(xq[r2t])).cuda()
     xs_d = torch.from_numpy(np.ascontiguousarray(xs[r2t])).cuda()
-    moe.moe_expert_ffn(xq_d, xs_d, offs, cfg.E, None, N, pw.struct(), None, 0, y, ws, wsb, err)
-    torch.cuda.synchronize()
+    if mode:
+        os.environ["MOE_B300_FFN_TILES"] = mode
+    try:
+        moe.moe_expert_ffn(xq_d, xs_d, offs, cfg.E, None, N, pw.struct(), None, 0, y, ws, wsb, err)
+        torch.cuda.synchronize()
+    finally:
+        os.environ.pop("MOE_B300_FFN_TILES", None)
     assert int(err.item()) == 0
     got = y.float().cpu().numpy()
     xdeq = O.dequantize_groups(xq, xs)[r2t]
@@ -70,18 +77,21 @@ def run_ffn_fp8(cfg, logits=None):
 SMALL = mi.config(4).scaled(T=300, d=256, E=8, I=256, R=4)
 
 
-def test_ffn_fp8_small():
-    run_ffn_fp8(SMALL)
+@pytest.mark.parametrize("mode", ["wide", "pair"])
+def test_ffn_fp8_small(mode):
+    run_ffn_fp8(SMALL, mode=mode)
 
 
-def test_ffn_fp8_skewed_groups_and_ragged_tiles():
+@pytest.mark.parametrize("mode", ["wide", "pair"])
+def test_ffn_fp8_skewed_groups_and_ragged_tiles(mode):
     cfg = SMALL.scaled(T=333, E=16, k=4, d=512, I=384, R=4)
     rng = np.random.default_rng(0)
     l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
     l[:, 2] += 6.0          # one expert takes nearly every token: many tiles, ragged tail
     l[:, 7] -= 20.0         # an expert that no token picks
-    run_ffn_fp8(cfg, logits=l)
+    run_ffn_fp8(cfg, logits=l, mode=mode)
 
 
-def test_ffn_fp8_single_token():
-    run_ffn_fp8(SMALL.scaled(T=1))
+@pytest.mark.parametrize("mode", ["wide", "pair"])
+def test_ffn_fp8_single_token(mode):
+    run_ffn_fp8(SMALL.scaled(T=1), mode=mode)
