@@ -54,10 +54,34 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// acc[i] = fma(v[i], f, acc[i]) for i < n (n even), two lanes per instruction
+// (fma.rn.f32x2: each element rounded once, as fmaf).
+template <int n>
+__device__ __forceinline__ void fma2_scaled(float *acc, const float *v, float f) {
+#pragma unroll
+  for (int i = 0; i < n; i += 2)
+    asm("{\n\t.reg .b64 a, x, s;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 s, {%4, %4};\n\t"
+        "fma.rn.f32x2 a, x, s, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(acc[i]), "+f"(acc[i + 1])
+        : "f"(v[i]), "f"(v[i + 1]), "f"(f));
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-// silu for the tensor-core epilogues, whose results are rounded to bf16 or e4m3:
-// the fast exponential and a reciprocal (z -> -inf gives z * 0 = -0).
-__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+// Reciprocal by the hardware approximation (rcp.approx.ftz.f32: about 1 ulp;
+// 1/inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// silu for the e4m3 epilogue, whose result is rounded to e4m3 (3 mantissa bits):
+// the fast exponential and the approximate reciprocal (z -> -inf gives z * 0 = -0).
+__device__ __forceinline__ float silu_fast(float z) { return z * rcp_approx(1.0f + __expf(-z)); }
 
 }  // namespace moe

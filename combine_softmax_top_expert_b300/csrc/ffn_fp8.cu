@@ -10,14 +10,14 @@
 // Two TMEM accumulators alternate so the tensor cores work on block kb+1 while the
 // epilogue folds block kb.
 //
-// This is the one-SM form, for few rows per expert; ffn_fp8_pair.cu holds the
-// SM-pair form used for many.  Tiles: A = 128 token rows, B = 256 weight rows (gate 128 + up 128 of
+// This is the one-SM form, for few rows per expert (and MOE_B300_FFN_TILES=swap or
+// wide); ffn_fp8_pair.cu holds the SM-pair form used for many.  Tiles: A = 128 token rows, B = 256 weight rows (gate 128 + up 128 of
 // one 128-feature block, or 256 output features of W_down), K blocks of 128 bytes.
 // 12 warps: warp 0 TMA, warp 1 MMA, warps 4-11 epilogue; epilogue warps w and w+4
 // share TMEM lanes (token rows) and split the 256 columns.
 //   gate/up  h = silu(g) * u for the tile's 128 features, quantised per row over
 //            exactly those 128 channels (the two halves exchange their amax through
-//            shared memory): scale = amax / 448, code = e4m3(h / scale).
+//            shared memory): scale = amax / 448, code = e4m3(h * (1 / scale)).
 //   down     y = acc, stored as bf16.
 #include "grouped.cuh"
 
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(d + c1 + 32, v + 32);
         tmem_wait_ld();
         fence_before();
-        mbar_arrive(dempty(b));  // the accumulator is in registers: let the next K block in
+        mbar_arrive_relaxed(dempty(b));  // the accumulator is in registers: let the next K block in
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc1[i] = fmaf(v[i], f1, acc1[i]);
       }
@@ -324,8 +324,7 @@ moe_status_t gate_up_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (!f.x_scales || !f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
   if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
-  // the one-SM tiles stay the default: the pair form loses more to the promotion chain
-  if (grouped::tile_kind(f.N, f.P, grouped::Tiles::kWide) == grouped::Tiles::kPair) return gate_up_e4m3_pair(f, st);
+  if (grouped::tile_kind(f.N, f.P) == grouped::Tiles::kPair) return gate_up_e4m3_pair(f, st);
   CUtensorMap m_x;
   if (!grouped::make_map(&m_x, f.x_perm, f.N, w.d, 1, 128)) return MOE_ERR_INVALID_ARG;
   if (!aligned(w.w13, 16)) return MOE_ERR_INVALID_ARG;
@@ -350,8 +349,7 @@ moe_status_t down_e4m3(const FfnArgs &f, cudaStream_t st) {
   if (!f.h_scales) return MOE_ERR_INVALID_ARG;
   const moe_weights_t &w = *f.w;
   if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;
-  // the one-SM tiles stay the default: the pair form loses more to the promotion chain
-  if (grouped::tile_kind(f.N, f.P, grouped::Tiles::kWide) == grouped::Tiles::kPair) return down_e4m3_pair(f, st);
+  if (grouped::tile_kind(f.N, f.P) == grouped::Tiles::kPair) return down_e4m3_pair(f, st);
   CUtensorMap m_h;
   if (!grouped::make_map(&m_h, f.h, f.N, w.I, 1, 128)) return MOE_ERR_INVALID_ARG;
   if (!aligned(w.w2, 16)) return MOE_ERR_INVALID_ARG;

@@ -4,25 +4,23 @@
 //
 // As in the one-SM kernel (ffn_fp8.cu), every 128-deep K block gets a fresh TMEM
 // accumulator that the epilogue warps fold into fp32 registers with the block's
-// scales, acc += D_kb * (s_row[kb] * s_weight_block[kb]).  That fold is a chain
-// (MMA, commit, TMEM load, release) that TMEM's two 256-column buffers must
-// cover.  Here a cluster of two CTAs owns a 256-token tile (128 rows per CTA) and
-// each K block is two independent groups of tcgen05.mma.cta_group::2 with
-// M = 256, N = 128, each committed and released on its own.  With four
-// 128-column half buffers in flight the chain is cut into shorter links, and
-// each SM loads only half of the weight rows, so a stage is 32 KB and six fit.
+// scales, acc += D_kb * (s_row[kb] * s_weight_block[kb]), and two 256-column
+// accumulators alternate.  Here a cluster of two CTAs owns a 256-token tile (128
+// rows per CTA): each K block is four tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 32) issued by the even CTA, and each SM loads only half of the weight rows,
+// so a stage is 32 KB and six fit.  (Splitting a K block into two separately
+// committed N = 128 groups was measured and is slower: every commit-and-wait hand-off
+// costs a few hundred cycles of issue time.)
 //
-// Group h of a K block (columns [128h, 128h+128) of its buffer):
-//   gate/up  the even CTA holds W_gate^T rows of the tile's 128 features, the
-//            odd CTA the W_up^T rows; group h reads rows [64h, 64h+64) of both,
-//            so its columns are gate then up of features [64h, 64h+64).
-//   down     the tile has 256 output features; CTA r holds rows [64r, 64r+64)
-//            of the two 128-feature weight tiles; group h reads tile h's rows
-//            of both CTAs, so column c is output feature c.
-// Epilogue warp w (w = 4..11) reads TMEM lanes 32*(w % 4).. of its own CTA and
-// group (w - 4) / 4: the same per-thread work as the one-SM kernel.
+// Weight rows of a tile, as in the bf16 pair kernel:
+//   gate/up  the even CTA holds W_gate^T rows of the tile's 128 features, the odd
+//            CTA the W_up^T rows: D columns 0-127 gate, 128-255 up.
+//   down     256 output features: the even CTA's 128 then the odd CTA's.
+// Epilogue warp w (w = 4..11) reads TMEM lanes 32*(w % 4).. of its own CTA; warps w
+// and w+4 split the columns (gate/up: features [64h, 64h+64) of gate and of up;
+// down: columns [128h, 128h+128)):
 //   gate/up  h = silu(g) * u for the tile's 128 features, quantised per row over
-//            those 128 channels (the two groups exchange their amax):
+//            those 128 channels (the two halves exchange their amax):
 //            scale = amax / 448, code = e4m3(h * (1 / scale)).
 //   down     y = acc, bf16.
 #include "grouped.cuh"
@@ -42,11 +40,12 @@ constexpr int kTokTile = 256;
 constexpr int kABytes = 128 * 128;  // this CTA's 128 token rows x 128 K bytes
 constexpr int kBBytes = 128 * 128;  // this CTA's 128 weight rows
 constexpr int kStage = kABytes + kBBytes;
-constexpr int kAccCols = 256;  // one K block = two 128-column groups
-constexpr int kGroupWarps = 4;  // epilogue warps per group per CTA
-// full[s], empty[s], dfull[b][h], dempty[b][h], drain, xbar
-constexpr int kBars = 2 * kStages + 4 + 4 + 2;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kBars * 8 + 16 + 2 * 256 * 4 +
+constexpr int kAccCols = 256;
+constexpr int kEpiWarps = 8;  // per CTA
+// full[s], empty[s], dfull[b], dempty[b], drain, xbar
+constexpr int kBars = 2 * kStages + 2 + 2 + 2;
+constexpr int kOutBox = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes staged for a TMA store
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kEpiWarps * kOutBox + kBars * 8 + 16 + 2 * 256 * 4 +
                          (grouped::kMaxGroups + 1) * 4;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 constexpr uint64_t kAbortSettleNs = 100000;
@@ -54,20 +53,21 @@ constexpr uint64_t kAbortSettleNs = 100000;
 template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_e4m3_pair(const Params p, const __grid_constant__ CUtensorMap tm_tok,
-                           const __grid_constant__ CUtensorMap tm_w) {
+                           const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStage);
+  uint8_t *out_box = smem + (size_t)kStages * kStage;  // [kEpiWarps][32 rows][64 bytes]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(out_box + kEpiWarps * kOutBox);
   int *misc = reinterpret_cast<int *>(bars + kBars);  // [0] TMEM base, [1] abort flag
   float *amax_x = reinterpret_cast<float *>(misc + 4);  // [2 tiles][2 groups][128 rows]
   int *tile_start = reinterpret_cast<int *>(amax_x + 512);
   const uint32_t stage0 = smem_u32(smem);
   auto full = [&](int s) { return smem_u32(&bars[s]); };  // used in the even CTA
   auto empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
-  auto dfull = [&](int b, int h) { return smem_u32(&bars[2 * kStages + 2 * b + h]); };
-  auto dempty = [&](int b, int h) { return smem_u32(&bars[2 * kStages + 4 + 2 * b + h]); };  // even CTA
-  const uint32_t drain = smem_u32(&bars[2 * kStages + 8]);
-  const uint32_t xbar = smem_u32(&bars[2 * kStages + 9]);
+  auto dfull = [&](int b) { return smem_u32(&bars[2 * kStages + b]); };
+  auto dempty = [&](int b) { return smem_u32(&bars[2 * kStages + 2 + b]); };  // used in the even CTA
+  const uint32_t drain = smem_u32(&bars[2 * kStages + 4]);
+  const uint32_t xbar = smem_u32(&bars[2 * kStages + 5]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -82,11 +82,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b)
-      for (int h = 0; h < 2; ++h) {
-        mbar_init(dfull(b, h), 1);
-        mbar_init(dempty(b, h), 2 * kGroupWarps);
-      }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(dfull(b), 1);
+      mbar_init(dempty(b), 2 * kEpiWarps);
+    }
     mbar_init(drain, 1);
     mbar_init(xbar, 256);
     misc[1] = 0;
@@ -95,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     tma_prefetch(&tm_tok);
     tma_prefetch(&tm_w);
+    tma_prefetch(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc2(smem_u32(&misc[0]), 2 * kAccCols);
@@ -118,12 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < total; tile += npairs) {
         const Tile t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
         const int e = max(t.e, 0);
-        // gated: rows [128r, +128) of the 256-row gate+up block; down: rows [64r, +64)
-        // of the two 128-row blocks of output features 256nt ..
-        // (the map holds fewer than 2^31 rows)
+        // gated: rows [128r, +128) of the 256-row gate+up block; down: the 128-row
+        // block of tile 2nt + r (the map holds fewer than 2^31 rows)
         int w0 = kGated ? ((e * p.w_tiles + t.nt) * KB * 256 + 128 * (int)rank)
-                        : ((e * p.w_tiles + 2 * t.nt) * KB * 128 + 64 * (int)rank);
-        const int w1 = KB * 128;  // down: the second tile's block, relative to the first
+                        : ((e * p.w_tiles + 2 * t.nt + (int)rank) * KB * 128);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
@@ -134,7 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rank == 0) mbar_expect_tx(full(s), 2 * kStage);
           tma_load_2d_pair(st, &tm_tok, bar, kb * 128, t.tok_row + 128 * (int)rank);
           tma_load_2d_pair(st + kABytes, &tm_w, bar, 0, w0);
-          if (!kGated) tma_load_2d_pair(st + kABytes + kBBytes / 2, &tm_w, bar, 0, w0 + w1);
           w0 += kGated ? 256 : 128;
           ++issued;
           if (++s == kStages) {
@@ -156,30 +153,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ MMA issuer (even CTA)
       int s = 0, gk = 0;
       uint32_t ph = 0;
-      const uint32_t id = idesc(256, 128, 0);
+      const uint32_t id = idesc(256, 256, 0);
       bool ok = true;
       for (int tile = pair; tile < total && ok; tile += npairs) {
         for (int kb = 0; kb < KB; ++kb, ++gk) {
           const int b = gk & 1;
-          if (!mbar_wait(full(s), ph, abort_flag, p.err)) {
+          if (!mbar_wait(full(s), ph, abort_flag, p.err) ||
+              !mbar_wait(dempty(b), ((gk >> 1) & 1) ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t a = stage0 + s * kStage, bb = a + kABytes;
+          fence_after();
+          const uint32_t a = stage0 + s * kStage, bb = a + kABytes, d = tmem + b * kAccCols;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(dempty(b, h), ((gk >> 1) & 1) ^ 1, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            fence_after();
-            const uint32_t d = tmem + b * kAccCols + h * 128;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8_2(d, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + h * (kBBytes / 2) + kk * 32), id, kk != 0);
-            commit2_both(dfull(b, h));
-          }
-          if (!ok) break;
+          for (int kk = 0; kk < 4; ++kk) mma_f8_2(d, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id, kk != 0);
+          commit2_both(dfull(b));
           commit2_both(empty(s));
           if (++s == kStages) {
             s = 0;
@@ -198,6 +186,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, half = (warp - 4) >> 2;
     const int r = q * 32 + lane;  // TMEM lane = this CTA's token row
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    // 64 bytes of output per row (w = 16 words) of this warp's 32 rows.  When all 32
+    // rows belong to the tile they go through this warp's staging box and one TMA
+    // store at column x (elements) of rows grow - lane ..; otherwise each row is
+    // written directly to `dst`.
+    uint8_t *box = out_box + (warp - 4) * kOutBox;
+    const uint32_t box_s = smem_u32(box);
+    auto store_rows = [&](const uint32_t *w, int x, bool ok, int grow, uint8_t *dst) {
+      if (__all_sync(kFull, ok)) {
+        if (lane == 0) bulk_wait_read();  // the previous store has read the box
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4 *>(box + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
+              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_out, box_s, x, grow);
+          bulk_commit();
+        }
+      } else if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          reinterpret_cast<uint4 *>(dst)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      }
+    };
+    // gated: gate columns [64h, +64) and up columns [128 + 64h, +64); down: [128h, +128)
+    const uint32_t c0 = kGated ? 64 * half : 128 * half;
+    const uint32_t c1 = kGated ? 128 + 64 * half : 128 * half + 64;
     int gk = 0, it = 0;
     for (int tile = pair; tile < total; tile += npairs, ++it) {
       const Tile t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sw0 = (e * wblocks + (kGated ? t.nt : 2 * t.nt + half)) * KB;
       const int sw1 = kGated ? (e * wblocks + p.feat / 128 + t.nt) * KB : sw0;
       const int sa = grow * KB;
-      float acc0[64], acc1[64];  // gated: gate, up of 64 features; down: 128 output features
+      float acc0[64], acc1[64];  // gated: gate, up of 64 features; down: columns c0.., c1..
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
       bool ok = true;
@@ -225,30 +242,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           s0_n = __ldg(p.w_scales + sw0 + kb + 1);
           if (kGated) s1_n = __ldg(p.w_scales + sw1 + kb + 1);
         }
-        if (!mbar_wait(dfull(b, half), (gk >> 1) & 1, abort_flag, p.err)) {
+        if (!mbar_wait(dfull(b), (gk >> 1) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         fence_after();
         const uint32_t d = lane_base + b * kAccCols;
         float v[64];
-        tmem_ld32(d + 128 * half, v);
-        tmem_ld32(d + 128 * half + 32, v + 32);
+        tmem_ld32(d + c0, v);
+        tmem_ld32(d + c0 + 32, v + 32);
         tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc0[i] = fmaf(v[i], f0, acc0[i]);
-        tmem_ld32(d + 128 * half + 64, v);
-        tmem_ld32(d + 128 * half + 96, v + 32);
+        fma2_scaled<64>(acc0, v, f0);
+        tmem_ld32(d + c1, v);
+        tmem_ld32(d + c1 + 32, v + 32);
         tmem_wait_ld();
         fence_before();
         __syncwarp();
-        // the group's columns are in registers: release them to the even CTA's MMA
+        // this warp's columns are in registers: release them to the even CTA's MMA
         if (lane == 0) {
-          if (rank == 0) mbar_arrive(dempty(b, half));
-          else mbar_arrive_cluster_relaxed(peer_addr(dempty(b, half), 0));
+          if (rank == 0) mbar_arrive_relaxed(dempty(b));
+          else mbar_arrive_cluster_relaxed(peer_addr(dempty(b), 0));
         }
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc1[i] = fmaf(v[i], f1, acc1[i]);
+        fma2_scaled<64>(acc1, v, f1);
       }
       if (!ok) break;
       if (t.e < 0 && r == 0 && half == 0 && rank == 0) raise_dev(p.err, MOE_DEV_LAYOUT);
@@ -270,44 +285,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // h is an intermediate: multiplying by 1/scale instead of dividing moves the
         // value before rounding by at most an fp32 ulp
         const float inv = __frcp_rn(scale);
-        if (row_ok) {
-          uint8_t *orow = static_cast<uint8_t *>(p.out) + (int64_t)grow * p.ld + t.nt * 128 + 64 * half;
+        uint32_t w[16];  // this row's 64 codes
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w[4];
+        for (int i = 0; i < 16; ++i)
+          w[i] = e4m3x2(acc0[4 * i] * inv, acc0[4 * i + 1] * inv) |
+                 (e4m3x2(acc0[4 * i + 2] * inv, acc0[4 * i + 3] * inv) << 16);
+        store_rows(w, t.nt * 128 + 64 * half, row_ok, grow, static_cast<uint8_t *>(p.out) + (int64_t)grow * p.ld +
+                                                            t.nt * 128 + 64 * half);
+        if (row_ok && half == 0) p.out_scales[(int64_t)grow * (p.feat / 128) + t.nt] = scale;
+      } else {
+        // four 32-column pieces of this thread's 128 output features
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int j = 16 * c + 4 * i;
-              w[i] = e4m3x2(acc0[j] * inv, acc0[j + 1] * inv) | (e4m3x2(acc0[j + 2] * inv, acc0[j + 3] * inv) << 16);
-            }
-            reinterpret_cast<uint4 *>(orow)[c] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          if (half == 0) p.out_scales[(int64_t)grow * (p.feat / 128) + t.nt] = scale;
-        }
-      } else if (row_ok) {
-        uint16_t *orow = static_cast<uint16_t *>(p.out) + (int64_t)grow * p.ld + t.nt * 256 + 128 * half;
+        for (int c = 0; c < 4; ++c) {
+          const float *a = c < 2 ? acc0 + 32 * c : acc1 + 32 * (c - 2);
+          uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 8 * c + 2 * i;
-            w[i] = pack_bf16x2(acc0[j], acc0[j + 1]);
-          }
-          reinterpret_cast<uint4 *>(orow)[c] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 8 * c + 2 * i;
-            w[i] = pack_bf16x2(acc1[j], acc1[j + 1]);
-          }
-          reinterpret_cast<uint4 *>(orow + 64)[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+          store_rows(w, t.nt * 256 + 128 * half + 32 * c, row_ok, grow,
+                     static_cast<uint8_t *>(p.out) + ((int64_t)grow * p.ld + t.nt * 256 + 128 * half + 32 * c) * 2);
         }
       }
     }
+    if (lane == 0) bulk_wait();
   }
   fence_before();
   __syncthreads();
@@ -320,9 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kGated>
-moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &w, cudaStream_t st) {
+moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &w, const CUtensorMap &o,
+                    cudaStream_t st) {
   static int pairs = 0;
-  return grouped::launch_pairs(grouped_gemm_e4m3_pair<kGated>, kThreads, kSmem, &pairs, st, p, a, w);
+  return grouped::launch_pairs(grouped_gemm_e4m3_pair<kGated>, kThreads, kSmem, &pairs, st, p, a, w, o);
 }
 
 }  // namespace
@@ -331,8 +331,9 @@ moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &w,
 // (d % 256 == 0, I % 128 == 0, no shared expert) and the scale pointers.
 moe_status_t gate_up_e4m3_pair(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
-  CUtensorMap m_x, m_w;
+  CUtensorMap m_x, m_w, m_h;
   if (!grouped::make_map(&m_x, f.x_perm, f.N, w.d, 1, 128)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_store_map(&m_h, f.h, f.N, w.I, 1, 32)) return MOE_ERR_INVALID_ARG;
   if (!grouped::make_map_tiled(&m_w, w.w13, (uint64_t)w.E_w * 2 * w.I * (w.d / 128), 128))
     return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
@@ -346,14 +347,15 @@ moe_status_t gate_up_e4m3_pair(const FfnArgs &f, cudaStream_t st) {
   p.a_scales = f.x_scales;
   p.w_scales = w.s13;
   p.out_scales = f.h_scales;
-  return launch<true>(p, m_x, m_w, st);
+  return launch<true>(p, m_x, m_w, m_h, st);
 }
 
 moe_status_t down_e4m3_pair(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
-  CUtensorMap m_h, m_w;
+  CUtensorMap m_h, m_w, m_y;
   if (!grouped::make_map(&m_h, f.h, f.N, w.I, 1, 128)) return MOE_ERR_INVALID_ARG;
-  if (!grouped::make_map_tiled(&m_w, w.w2, (uint64_t)w.E_w * w.d * (w.I / 128), 64)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_store_map(&m_y, f.y, f.N, w.d, 2, 32)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_map_tiled(&m_w, w.w2, (uint64_t)w.E_w * w.d * (w.I / 128), 128)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)w.d;
   p.K = (int)w.I;
@@ -364,7 +366,7 @@ moe_status_t down_e4m3_pair(const FfnArgs &f, cudaStream_t st) {
   p.ld = w.d;
   p.a_scales = f.h_scales;
   p.w_scales = w.s2;
-  return launch<false>(p, m_h, m_w, st);
+  return launch<false>(p, m_h, m_w, m_y, st);
 }
 
 }  // namespace moe

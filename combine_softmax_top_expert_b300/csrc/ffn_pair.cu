@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (rank == 0) mbar_arrive(tempty(b));
+        if (rank == 0) mbar_arrive_relaxed(tempty(b));
         else mbar_arrive_cluster_relaxed(b ? tempty_even1 : tempty_even0);
       }
     }

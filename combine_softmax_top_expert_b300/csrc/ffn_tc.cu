@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_before();
-      mbar_arrive(tempty(b));
+      mbar_arrive_relaxed(tempty(b));
     }
   }
   fence_before();

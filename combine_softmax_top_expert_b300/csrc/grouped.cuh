@@ -174,6 +174,20 @@ inline bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t c
          CUDA_SUCCESS;
 }
 
+// 2-D map for TMA stores of a row-major [rows, cols] output: boxes of box_rows rows
+// x 64 bytes, 64-byte swizzle (16-byte chunk c of box row r at c ^ ((r / 2) % 4)).
+inline bool make_store_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, int esize, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0 || !aligned(base, 16) || (cols * esize) % 16) return false;
+  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / esize), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over packed (tiled, already swizzled) weights seen as `rows` rows of 128
 // bytes; boxes of box_rows rows copied as they are (no swizzle).  Row
 // ((e * w_tiles + t) * KB + kb) * tile_rows + i is row i of weight_block(e, t, kb).
@@ -234,12 +248,12 @@ moe_status_t launch_pairs(void (*kernel)(KArgs...), int threads, size_t smem, in
 // otherwise; "wide" is the one-SM form of pair.  The environment variable
 // MOE_B300_FFN_TILES=swap|wide|pair overrides the choice.
 enum class Tiles { kSwap, kWide, kPair };
-inline Tiles tile_kind(int64_t N, int64_t P, Tiles many_rows = Tiles::kPair) {
+inline Tiles tile_kind(int64_t N, int64_t P) {
   const char *env = std::getenv("MOE_B300_FFN_TILES");
   if (env && !std::strcmp(env, "swap")) return Tiles::kSwap;
   if (env && !std::strcmp(env, "wide")) return Tiles::kWide;
   if (env && !std::strcmp(env, "pair")) return Tiles::kPair;
-  return N < 64 * P ? Tiles::kSwap : many_rows;
+  return N < 64 * P ? Tiles::kSwap : Tiles::kPair;
 }
 
 inline Params base_params(const FfnArgs &f) {
