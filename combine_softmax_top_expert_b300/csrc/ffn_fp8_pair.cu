@@ -191,21 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // store at column x (elements) of rows grow - lane ..; otherwise each row is
     // written directly to `dst`.
     uint8_t *box = out_box + (warp - 4) * kOutBox;
-    const uint32_t box_s = smem_u32(box);
     auto store_rows = [&](const uint32_t *w, int x, bool ok, int grow, uint8_t *dst) {
       if (__all_sync(kFull, ok)) {
         if (lane == 0) bulk_wait_read();  // the previous store has read the box
         __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4 *>(box + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
-              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tm_out, box_s, x, grow);
-          bulk_commit();
-        }
+        warp_store_box(&tm_out, box, w, x, grow, lane);
       } else if (ok) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)

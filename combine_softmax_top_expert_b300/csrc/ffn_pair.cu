@@ -35,7 +35,9 @@ constexpr int kStage = kABytes + kBBytes;
 constexpr int kAccCols = 256;
 constexpr int kEpiWarps = 4;
 constexpr int kBars = 2 * kStages + 5;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kBars * 8 + 16 + (grouped::kMaxGroups + 1) * 4;
+constexpr int kOutBox = 32 * 64;  // 32 rows x 64 bytes staged for a TMA store; two per epilogue warp
+constexpr size_t kSmem =
+    1024 + (size_t)kStages * kStage + 2 * kEpiWarps * kOutBox + kBars * 8 + 16 + (grouped::kMaxGroups + 1) * 4;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 // After an abort a CTA cannot see its own copies land (they complete on the even
@@ -45,10 +47,12 @@ constexpr uint64_t kAbortSettleNs = 100000;
 template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_pair(const Params p, const __grid_constant__ CUtensorMap tm_tok,
-                           const __grid_constant__ CUtensorMap tm_sh, const __grid_constant__ CUtensorMap tm_w) {
+                           const __grid_constant__ CUtensorMap tm_sh, const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStage);
+  uint8_t *out_box = smem + (size_t)kStages * kStage;  // [kEpiWarps][2][32 rows][64 bytes]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(out_box + 2 * kEpiWarps * kOutBox);
   int *misc = reinterpret_cast<int *>(bars + kBars);  // [0] TMEM base, [1] abort flag
   int *tile_start = misc + 4;
   const uint32_t stage0 = smem_u32(smem);
@@ -83,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_tok);
     tma_prefetch(&tm_sh);
     tma_prefetch(&tm_w);
+    tma_prefetch(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc2(smem_u32(&misc[0]), 2 * kAccCols);
@@ -174,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;  // TMEM lane = this CTA's token row
     const uint32_t tempty_even0 = peer_addr(tempty(0), 0), tempty_even1 = peer_addr(tempty(1), 0);
+    uint8_t *boxes = out_box + (warp - 2) * 2 * kOutBox;
+    int nbox = 0;  // TMA stores this warp has issued; they alternate between its two boxes
     int it = 0;
     for (int tile = pair; tile < total; tile += npairs, ++it) {
       const Tile t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
@@ -185,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = 128 * (int)rank + r;
       const bool ok = row < t.valid && t.e >= 0;
       uint16_t *orow = out + (int64_t)(t.out_row + (ok ? row : 0)) * p.ld + (int64_t)t.nt * (kGated ? 128 : 256);
+      // all 32 rows of this warp belong to the tile: stage each 32-column piece and
+      // store it with TMA (two boxes in flight); otherwise store row by row
+      const bool whole = __all_sync(kFull, ok);
       constexpr int kChunks = kGated ? 4 : 8;
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
@@ -202,7 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pk[i] = pack_bf16x2(a0, a1);
         }
-        if (ok) {
+        if (whole) {
+          if (lane == 0) bulk_wait_read_1();  // the store that last used this box has read it
+          __syncwarp();
+          warp_store_box(&tm_out, boxes + (nbox & 1) * kOutBox, pk, t.nt * (kGated ? 128 : 256) + 32 * c,
+                         t.out_row + row, lane);
+          ++nbox;
+        } else if (ok) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -215,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mbar_arrive_cluster_relaxed(b ? tempty_even1 : tempty_even0);
       }
     }
+    if (lane == 0) bulk_wait();
   }
   fence_before();
   __syncthreads();
@@ -228,9 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kGated>
 moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &sh, const CUtensorMap &w,
-                    cudaStream_t st) {
+                    const CUtensorMap &o, cudaStream_t st) {
   static int pairs = 0;
-  return grouped::launch_pairs(grouped_gemm_bf16_pair<kGated>, kThreads, kSmem, &pairs, st, p, a, sh, w);
+  return grouped::launch_pairs(grouped_gemm_bf16_pair<kGated>, kThreads, kSmem, &pairs, st, p, a, sh, w, o);
 }
 
 }  // namespace
@@ -239,7 +256,7 @@ moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &sh
 moe_status_t gate_up_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I;
-  CUtensorMap m_x, m_sh, m_w;
+  CUtensorMap m_x, m_sh, m_w, m_h;
   const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
   const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
   if (!grouped::make_map(&m_x, xsrc, xrows, d, 2, 128)) return MOE_ERR_INVALID_ARG;
@@ -248,6 +265,7 @@ moe_status_t gate_up_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   } else {
     m_sh = m_x;
   }
+  if (!grouped::make_store_map(&m_h, f.h, f.N + f.T_shared, I, 2, 32)) return MOE_ERR_INVALID_ARG;
   // the packed W_gate^T/W_up^T as 128-byte rows
   if (!grouped::make_map_tiled(&m_w, w.w13, (uint64_t)w.E_w * 2 * I * (d / 64), 128)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
@@ -259,7 +277,7 @@ moe_status_t gate_up_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   p.shared_row0 = 0;
   p.out = f.h;
   p.ld = I;
-  return launch<true>(p, m_x, m_sh, m_w, st);
+  return launch<true>(p, m_x, m_sh, m_w, m_h, st);
 }
 
 // Needs d % 256 == 0 (256 output features per pair tile).
@@ -267,8 +285,9 @@ moe_status_t down_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
   if (d % 256) return MOE_ERR_UNSUPPORTED;
-  CUtensorMap m_h, m_w;
+  CUtensorMap m_h, m_w, m_y;
   if (!grouped::make_map(&m_h, f.h, rows, I, 2, 128)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_store_map(&m_y, f.y, rows, d, 2, 32)) return MOE_ERR_INVALID_ARG;
   if (!grouped::make_map_tiled(&m_w, w.w2, (uint64_t)w.E_w * d * (I / 64), 128)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)d;
@@ -279,7 +298,7 @@ moe_status_t down_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   p.shared_row0 = (int)f.N;
   p.out = f.y;
   p.ld = d;
-  return launch<false>(p, m_h, m_h, m_w, st);
+  return launch<false>(p, m_h, m_h, m_w, m_y, st);
 }
 
 }  // namespace moe

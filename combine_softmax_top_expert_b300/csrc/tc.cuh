@@ -126,6 +126,27 @@ __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_g
 // Make this thread's generic-proxy shared-memory writes visible to TMA.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// A warp writes 64 bytes of each of 32 consecutive output rows (lane i: row y0 + i,
+// its 16 words w) into `box` (2 KB of shared memory, 64-byte swizzle: chunk c of
+// row i at c ^ ((i / 2) % 4), which keeps the 16-byte writes free of bank
+// conflicts) and lane 0 stores the box with TMA at column x.  The caller makes sure
+// no earlier store still reads `box` (bulk_wait_read of lane 0, then __syncwarp).
+__device__ __forceinline__ void warp_store_box(const CUtensorMap *m, uint8_t *box, const uint32_t *w, int x, int y0,
+                                               int lane) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4 *>(box + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(m, smem_u32(box), x, y0);
+    bulk_commit();
+  }
+}
+// As bulk_wait_read, leaving the most recent store still reading.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // Contiguous global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte
 // aligned), completing on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
