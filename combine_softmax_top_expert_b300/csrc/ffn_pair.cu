@@ -3,17 +3,21 @@
 // is one more always-on group).  The tile orientation for many rows per expert.
 //
 // A cluster of two CTAs owns one 256-token x 256-weight-row tile: CTA r loads
-// token rows [128r, 128r+128) and weight rows [128r, 128r+128) of every K block
-// into its own shared memory, and the even CTA issues tcgen05.mma.cta_group::2
-// (M = 256, N = 256) that reads both CTAs' operands and leaves D rows
-// [128r, +128) in CTA r's TMEM.  Per SM that is the MMA rate of a 128 x 256 tile
-// with half of the weight traffic into shared memory, so a 32 KB stage feeds as
-// many tensor cycles as a 48 KB stage of a one-SM tile and six stages fit.
-//   gate/up   weight rows 0-127 = W_gate^T of 128 features (even CTA), 128-255 =
-//             W_up^T of the same features (odd CTA): D columns 0-127 gate, 128-255
-//             up; h = silu(gate) * up, bf16.
-//   down      weight rows = 256 output features (the even CTA's 128, then the
-//             odd CTA's); y bf16.
+// token rows [128r, 128r+128) and 128 of the weight rows of every K block into its
+// own shared memory, and the even CTA issues tcgen05.mma.cta_group::2 (M = 256,
+// N = 256) that reads both CTAs' operands and leaves D rows [128r, +128) in CTA r's
+// TMEM (columns 0-127 from the even CTA's weight rows, 128-255 from the odd CTA's).
+// Per SM that is the MMA rate of a 128 x 256 tile with half of the weight traffic
+// into shared memory, so a 32 KB stage feeds as many tensor cycles as a 48 KB stage
+// of a one-SM tile and six stages fit.
+// A group's last tile, when it holds at most 128 rows, is a half tile: M = 128, CTA
+// r supplies token rows [64r, 64r+64) (the first 64 rows of its A stage) and its TMEM
+// lanes 0-63 get those rows x columns 0-127, lanes 64-127 the same rows x columns
+// 128-255 -- half the MMA work instead of padding to 256 rows.
+//   gate/up   CTA r holds W_gate^T then W_up^T rows of features [64r, 64r+64) of
+//             the tile's 128, so a 128-column half of D is gate then up of 64
+//             features; h = silu(gate) * up, bf16.
+//   down      CTA r holds the 128 weight rows of output features [128r, +128); y bf16.
 // Roles per CTA: warp 0 TMA (both CTAs; all copies complete on the even CTA's
 // stage barrier), warp 1 MMA (even CTA; TMEM allocation in both), warps 2-5
 // epilogue (both CTAs, each its own 128 rows).
@@ -110,10 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
       const CUtensorMap *tmt = (kGated && t.shared) ? &tm_sh : &tm_tok;
       const int e = max(t.e, 0);
-      // first row of this CTA's half of the K-block-0 weight block
+      // first weight row of this CTA in the K-block-0 block: gated, the gate rows of
+      // features [64r, +64) (the up rows follow 128 rows later); down, tile 2nt + r
       const int wt = kGated ? t.nt : 2 * t.nt + (int)rank;
       const int wrows = kGated ? 256 : 128;
-      const int64_t w0 = ((int64_t)e * p.w_tiles + wt) * KB * wrows + (kGated ? 128 * rank : 0);
+      const int64_t w0 = ((int64_t)e * p.w_tiles + wt) * KB * wrows + (kGated ? 64 * rank : 0);
+      const int a_row = t.tok_row + (t.half ? 64 : 128) * (int)rank;
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
@@ -122,8 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = stage0 + s * kStage, bar = peer_addr(full(s), 0);
         if (rank == 0) mbar_expect_tx(full(s), 2 * kStage);
-        tma_load_2d_pair(st, tmt, bar, kb * 64, t.tok_row + 128 * (int)rank);
-        tma_load_2d_pair(st + kABytes, &tm_w, bar, 0, (int)(w0 + (int64_t)kb * wrows));
+        tma_load_2d_pair(st, tmt, bar, kb * 64, a_row);
+        const int wr = (int)(w0 + (int64_t)kb * wrows);
+        if (kGated) {
+          tma_load_2d_pair(st + kABytes, &tm_w, bar, 0, wr);
+          tma_load_2d_pair(st + kABytes + kBBytes / 2, &tm_w, bar, 0, wr + 128);
+        } else {
+          tma_load_2d_pair(st + kABytes, &tm_w, bar, 0, wr);
+        }
         ++issued;
         if (++s == kStages) {
           s = 0;
@@ -144,8 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ MMA issuer (even CTA)
     int s = 0, it = 0;
     uint32_t ph = 0;
-    const uint32_t id = idesc(256, 256, 1);
     for (int tile = pair; tile < total; tile += npairs, ++it) {
+      const Tile t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
+      const uint32_t id = idesc(t.half ? 128 : 256, 256, 1);
       const int b = it & 1;
       if (!mbar_wait(tempty(b), ((it >> 1) & 1) ^ 1, abort_flag, p.err)) break;
       fence_after();
@@ -189,18 +202,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       if (t.e < 0 && r == 0 && rank == 0) raise_dev(p.err, MOE_DEV_LAYOUT);
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * kAccCols;
-      const int row = 128 * (int)rank + r;
+      // full tile: lane r is token row 128*rank + r and holds all 256 columns.
+      // half tile: lane r is token row 64*rank + r % 64 and holds the 128 columns of
+      // feature half r / 64 (in TMEM columns 0-127).
+      const bool hv = t.half;
+      const int row = hv ? 64 * (int)rank + (r & 63) : 128 * (int)rank + r;
       const bool ok = row < t.valid && t.e >= 0;
-      uint16_t *orow = out + (int64_t)(t.out_row + (ok ? row : 0)) * p.ld + (int64_t)t.nt * (kGated ? 128 : 256);
+      const int fbase = hv ? (r >> 6) * (kGated ? 64 : 128) : 0;  // first output feature
+      uint16_t *orow =
+          out + (int64_t)(t.out_row + (ok ? row : 0)) * p.ld + (int64_t)t.nt * (kGated ? 128 : 256) + fbase;
       // all 32 rows of this warp belong to the tile: stage each 32-column piece and
       // store it with TMA (two boxes in flight); otherwise store row by row
       const bool whole = __all_sync(kFull, ok);
-      constexpr int kChunks = kGated ? 4 : 8;
+      const int nchunks = (kGated ? 4 : 8) >> (hv ? 1 : 0);
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = 0; c < nchunks; ++c) {
+        // gated: gate columns of features fbase + 32c .. (the up columns are 64 later)
+        const int col = kGated ? ((hv || c < 2) ? 32 * c : 128 + 32 * (c - 2)) : 32 * c;
         float v[32], u[32];
-        tmem_ld32(tb + 32 * c, v);
-        if (kGated) tmem_ld32(tb + 128 + 32 * c, u);
+        tmem_ld32(tb + col, v);
+        if (kGated) tmem_ld32(tb + col + 64, u);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -215,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (whole) {
           if (lane == 0) bulk_wait_read_1();  // the store that last used this box has read it
           __syncwarp();
-          warp_store_box(&tm_out, boxes + (nbox & 1) * kOutBox, pk, t.nt * (kGated ? 128 : 256) + 32 * c,
+          warp_store_box(&tm_out, boxes + (nbox & 1) * kOutBox, pk, t.nt * (kGated ? 128 : 256) + fbase + 32 * c,
                          t.out_row + row, lane);
           ++nbox;
         } else if (ok) {
@@ -267,7 +288,7 @@ moe_status_t gate_up_bf16_pair(const FfnArgs &f, cudaStream_t st) {
   }
   if (!grouped::make_store_map(&m_h, f.h, f.N + f.T_shared, I, 2, 32)) return MOE_ERR_INVALID_ARG;
   // the packed W_gate^T/W_up^T as 128-byte rows
-  if (!grouped::make_map_tiled(&m_w, w.w13, (uint64_t)w.E_w * 2 * I * (d / 64), 128)) return MOE_ERR_INVALID_ARG;
+  if (!grouped::make_map_tiled(&m_w, w.w13, (uint64_t)w.E_w * 2 * I * (d / 64), 64)) return MOE_ERR_INVALID_ARG;
   Params p = grouped::base_params(f);
   p.feat = (int)I;
   p.K = (int)d;

@@ -45,6 +45,7 @@ struct Params {
 struct Tile {
   int e, tok_row, out_row, valid, nt;
   bool shared;
+  bool half;  // SM-pair tiles (256 tokens): the group's last tile holds at most 128 rows
 };
 
 // The packed weights are tiled: for expert e, tile t and K block kb (128 bytes
@@ -140,6 +141,7 @@ __device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, i
   t.e = e;
   t.nt = nt;
   t.valid = min(kTokTile, n - mt * kTokTile);
+  t.half = kTokTile == 256 && t.valid <= 128;
   t.tok_row = (t.shared ? p.shared_row0 : r0) + mt * kTokTile;
   t.out_row = (t.shared ? p.N : r0) + mt * kTokTile;
   return t;
