@@ -15,7 +15,7 @@ __all__ = [
     "MoeError", "lib", "library_path", "MOE_F32", "MOE_BF16", "MOE_E4M3",
     "MOE_DEV_NONFINITE_LOGIT", "MOE_DEV_ID_RANGE", "MOE_DEV_TIMEOUT", "MOE_DEV_LAYOUT",
     "LoadStats", "Eplb", "Weights", "Shape", "LayerAux",
-    "moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
+    "moe_status_string", "moe_route", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
     "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error", "EXPORTED",
@@ -30,7 +30,7 @@ MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 << 20
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
 
-EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_dispatch_workspace_size",
+EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
             "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error")
@@ -52,7 +52,8 @@ class LoadStats(ctypes.Structure):
 
 
 class Eplb(ctypes.Structure):
-    _fields_ = [("P", c_i32), ("phys_to_logical", c_vp), ("replica_count", c_vp), ("logical_to_phys", c_vp)]
+    _fields_ = [("P", c_i32), ("phys_to_logical", c_vp), ("replica_count", c_vp), ("logical_to_phys", c_vp),
+                ("max_replicas", c_i32)]
 
 
 class Weights(ctypes.Structure):
@@ -62,7 +63,8 @@ class Weights(ctypes.Structure):
 
 class Shape(ctypes.Structure):
     _fields_ = [("T", c_i64), ("d", c_i64), ("E", c_i64), ("I", c_i64), ("k", c_i32), ("R", c_i32),
-                ("n_redundant", c_i32), ("shared", c_i32), ("act_dtype", c_i32), ("expert_dtype", c_i32)]
+                ("n_redundant", c_i32), ("shared", c_i32), ("act_dtype", c_i32), ("expert_dtype", c_i32),
+                ("eplb_placement", c_i32)]
 
 
 class LayerAux(ctypes.Structure):
@@ -71,7 +73,7 @@ class LayerAux(ctypes.Structure):
                                     "phys_to_logical", "phys_rank", "replica_count", "logical_to_phys")]
 
 
-assert ctypes.sizeof(LoadStats) == 32 and ctypes.sizeof(Weights) == 64 and ctypes.sizeof(Shape) == 56
+assert ctypes.sizeof(LoadStats) == 32 and ctypes.sizeof(Weights) == 64 and ctypes.sizeof(Shape) == 64
 
 # ------------------------------------------------------------------ loading
 _lib = None
@@ -92,6 +94,7 @@ def lib():
             "moe_last_cuda_error": (ctypes.c_char_p, []),
             "moe_route": (st, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+            "moe_eplb_balanced_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
             "moe_dispatch_layout": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
                                     + [c_vp, sz, c_vp, c_vp]),
@@ -159,6 +162,13 @@ def moe_eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, 
                  stream=None):
     _check("moe_eplb_map", lib().moe_eplb_map(_p(logical_counts), E, R, n_redundant, _p(phys_to_logical),
                                               _p(phys_rank), _p(replica_count), _p(logical_to_phys), _s(stream)))
+
+
+def moe_eplb_balanced_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
+                          logical_to_phys, rank_load=None, stream=None):
+    _check("moe_eplb_balanced_map",
+           lib().moe_eplb_balanced_map(_p(logical_counts), E, R, n_redundant, _p(phys_to_logical), _p(phys_rank),
+                                       _p(replica_count), _p(logical_to_phys), _p(rank_load), _s(stream)))
 
 
 def moe_dispatch_workspace_size(T, k, P) -> int:

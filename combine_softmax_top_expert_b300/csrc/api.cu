@@ -10,6 +10,8 @@ size_t dispatch_ws_bytes(int64_t T, int32_t k, int64_t P);
 moe_status_t dispatch_layout(const int32_t *, int64_t, int32_t, int64_t, int32_t, const moe_eplb_t *, int32_t *,
                              int32_t *, int32_t *, int32_t *, int32_t *, int32_t *, int32_t *, moe_load_stats_t *,
                              void *, size_t, int32_t *, cudaStream_t);
+moe_status_t eplb_balanced_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *,
+                               int32_t *, double *, cudaStream_t);
 moe_status_t eplb_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *, int32_t *,
                       cudaStream_t);
 moe_status_t permute(const void *, moe_dtype_t, int64_t, int64_t, int32_t, const int32_t *, void *, moe_dtype_t,
@@ -95,7 +97,7 @@ struct LayerPlan {
   int64_t T, N, P, d, I, E;
   int32_t k, R;
   size_t act_bytes, perm_bytes, y_bytes;
-  bool eplb, shared;
+  bool eplb, shared, balanced;
   // byte offsets into the workspace
   size_t o_ids, o_w, o_lc, o_pc, o_po, o_rc, o_ro, o_r2t, o_s2r, o_stats, o_p2l, o_prank, o_repc, o_l2p, o_disp,
       o_xp, o_xs, o_y, o_ffn, total;
@@ -114,6 +116,8 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
   p->I = s->I;
   p->N = s->T * s->k;
   p->eplb = s->n_redundant > 0;
+  if (s->eplb_placement != 0 && s->eplb_placement != 1) return false;
+  p->balanced = p->eplb && s->eplb_placement == 1;
   p->shared = s->shared != 0;
   p->P = s->E + s->n_redundant;
   p->act_bytes = s->act_dtype == MOE_F32 ? 4 : 2;
@@ -139,7 +143,7 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
   p->o_p2l = take((size_t)p->P * 4);
   p->o_prank = take((size_t)p->P * 4);
   p->o_repc = take((size_t)p->E * 4);
-  p->o_l2p = take((size_t)p->E * 8);
+  p->o_l2p = take((size_t)p->E * 4 * (p->balanced ? 1 + s->n_redundant : 2));
   p->o_disp = take(dispatch_ws_bytes(p->T, p->k, p->P));
   p->o_xp = take((size_t)p->N * p->d * p->perm_bytes);
   p->o_xs = take(s->expert_dtype == MOE_E4M3 ? (size_t)p->N * (p->d / 128) * 4 : 0);
@@ -258,13 +262,15 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
 
   moe_status_t r;
   if ((r = moe_route(logits, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK) return r;
-  moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p};
+  moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p, p.balanced ? (int32_t)(1 + p.P - p.E) : 2};
   if (p.eplb) {
     // counts of this batch's logical routing, then the replica map built on them
     if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, nullptr, lc, pc, po, rc, ro, r2t, s2r, stats, disp,
                              disp_bytes, err, st)) != MOE_OK)
       return r;
-    if ((r = eplb_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p2l, prank, repc, l2p, st)) != MOE_OK) return r;
+    r = p.balanced ? eplb_balanced_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p2l, prank, repc, l2p, nullptr, st)
+                   : eplb_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p2l, prank, repc, l2p, st);
+    if (r != MOE_OK) return r;
   }
   if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.eplb ? &map : nullptr, lc, pc, po, rc, ro, r2t, s2r, stats,
                            disp, disp_bytes, err, st)) != MOE_OK)

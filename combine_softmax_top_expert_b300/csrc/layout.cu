@@ -33,7 +33,8 @@ struct PhysMap {
   int E;
   int k;
   const int32_t *replica_count;    // null: identity map
-  const int32_t *logical_to_phys;  // [E, 2]
+  const int32_t *logical_to_phys;  // [E, stride]
+  int stride;
 };
 
 __device__ __forceinline__ int phys_of(const int32_t *ids, int64_t s, const PhysMap &m, int32_t *err) {
@@ -45,7 +46,7 @@ __device__ __forceinline__ int phys_of(const int32_t *ids, int64_t s, const Phys
   if (!m.replica_count) return e;
   const int64_t t = s / m.k;
   const int rc = m.replica_count[e];
-  return m.logical_to_phys[2 * e + (int)(t % rc)];
+  return m.logical_to_phys[m.stride * e + (int)(t % rc)];
 }
 
 __global__ void __launch_bounds__(256) layout_count_kernel(const int32_t *__restrict__ ids, int64_t N, int P,
@@ -262,6 +263,112 @@ __global__ void __launch_bounds__(1024) eplb_map_kernel(const int32_t *__restric
   }
 }
 
+// The page's load-aware placement ("6.4 ...", section 5.2) as a physical-expert map.
+// One CTA of 1024 threads; E <= 1024, P = E + n_red <= 2048, R <= 1024.
+// Loads per replica are count / replicas.  Comparisons between them use exact
+// cross-multiplication, a/b > c/d <=> a*d > c*b: with counts below 2^31 and at most
+// 1025 replicas two different quotients differ by at least 1/1025^2, more than an
+// fp64 ulp of any of them, so the correctly rounded fp64 quotients the page's
+// procedure compares are ordered the same way (and equal only when exactly equal).
+// The per-rank loads are summed in fp64 in the procedure's order, so the map and the
+// loads are exactly the ones it gives.
+__device__ __forceinline__ bool heavier(int64_t ca, int ra, int ia, int64_t cb, int rb, int ib) {
+  const int64_t l = ca * rb, r = cb * ra;
+  return l > r || (l == r && ia < ib);
+}
+
+__global__ void __launch_bounds__(1024) eplb_balanced_kernel(const int32_t *__restrict__ counts, int E, int R,
+                                                             int n_red, int32_t *phys_to_logical, int32_t *phys_rank,
+                                                             int32_t *replica_count, int32_t *logical_to_phys,
+                                                             int stride, double *rank_load) {
+  __shared__ int32_t cnt[1024], rep[1024];
+  __shared__ double per[1024];              // load of one replica of expert e
+  __shared__ int16_t oe[kMaxP], oj[kMaxP];  // replicas in placement order: expert, replica index
+  __shared__ double load[1024];             // per rank
+  __shared__ int32_t used[1024];            // slots taken per rank
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = E + n_red, S = P / R;
+  for (int e = tid; e < E; e += blockDim.x) {
+    cnt[e] = counts[e];
+    rep[e] = 1;
+  }
+  for (int r = tid; r < R; r += blockDim.x) {
+    load[r] = 0.0;
+    used[r] = 0;
+  }
+  for (int i = tid; i < E * stride; i += blockDim.x) logical_to_phys[i] = -1;
+  __syncthreads();
+  // 1. each redundant slot to the expert with the highest load per replica (lowest
+  // index on a tie); one warp, so no block barrier per slot
+  if (warp == 0) {
+    for (int it = 0; it < n_red; ++it) {
+      int bi = -1;
+      for (int e = lane; e < E; e += 32)
+        if (bi < 0 || heavier(cnt[e], rep[e], e, cnt[bi], rep[bi], bi)) bi = e;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        if (oi >= 0 && (bi < 0 || heavier(cnt[oi], rep[oi], oi, cnt[bi], rep[bi], bi))) bi = oi;
+      }
+      if (lane == 0) rep[bi] += 1;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // 2. replicas heaviest first; equal loads keep expert order, then replica order
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int64_t ce = cnt[e];
+    const int re = rep[e];
+    int pos = 0;
+    for (int f = 0; f < E; ++f) pos += heavier(cnt[f], rep[f], f, ce, re, e) ? rep[f] : 0;
+    for (int j = 0; j < re; ++j) {
+      oe[pos + j] = (int16_t)e;
+      oj[pos + j] = (int16_t)j;
+    }
+    replica_count[e] = re;
+    per[e] = (double)ce / (double)re;
+  }
+  __syncthreads();
+  // 3. each replica onto the lightest rank with a free slot (lowest rank on a tie).
+  // The loads are non-negative doubles, whose bit patterns order like the values, so
+  // they are compared as 64-bit integers.
+  if (warp == 0) {
+    for (int p = 0; p < P; ++p) {
+      int64_t bv = 0;
+      int bg = -1;
+      for (int r = lane; r < R; r += 32) {
+        const int64_t v = __double_as_longlong(load[r]);
+        if (used[r] < S && (bg < 0 || v < bv)) {
+          bv = v;
+          bg = r;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int64_t ov = __shfl_down_sync(kFull, bv, o);
+        const int og = __shfl_down_sync(kFull, bg, o);
+        if (og >= 0 && (bg < 0 || ov < bv || (ov == bv && og < bg))) {
+          bv = ov;
+          bg = og;
+        }
+      }
+      if (lane == 0) {
+        const int e = oe[p], j = oj[p];
+        const int pid = bg * S + used[bg];
+        load[bg] += per[e];
+        used[bg] += 1;
+        phys_to_logical[pid] = e;
+        phys_rank[pid] = bg;
+        logical_to_phys[stride * e + j] = pid;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (rank_load)
+    for (int r = tid; r < R; r += blockDim.x) rank_load[r] = load[r];
+}
+
 }  // namespace
 
 size_t dispatch_ws_bytes(int64_t T, int32_t k, int64_t P) {
@@ -290,7 +397,8 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
   int32_t *hist = static_cast<int32_t *>(ws);
   int32_t *chunk_rank = reinterpret_cast<int32_t *>(static_cast<char *>(ws) +
                                                     align_up((size_t)chunks * P * 4, 256));
-  PhysMap m{(int)E, k, eplb ? eplb->replica_count : nullptr, eplb ? eplb->logical_to_phys : nullptr};
+  PhysMap m{(int)E, k, eplb ? eplb->replica_count : nullptr, eplb ? eplb->logical_to_phys : nullptr,
+            eplb && eplb->max_replicas > 0 ? eplb->max_replicas : 2};
   if (chunks > 0) {
     const size_t smem = (size_t)kCountWarps * P * 4;
     if (smem > 48 * 1024) {
@@ -319,6 +427,18 @@ moe_status_t eplb_map(const int32_t *logical_counts, int64_t E, int32_t R, int32
   return launch_status();
 }
 
+moe_status_t eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_red,
+                               int32_t *phys_to_logical, int32_t *phys_rank, int32_t *replica_count,
+                               int32_t *logical_to_phys, double *rank_load, cudaStream_t st) {
+  if (E < 1 || E > 1024 || R < 1 || R > 1024 || n_red < 0 || E + n_red > kMaxP || (E + n_red) % R)
+    return MOE_ERR_INVALID_ARG;
+  if (!logical_counts || !phys_to_logical || !phys_rank || !replica_count || !logical_to_phys)
+    return MOE_ERR_INVALID_ARG;
+  eplb_balanced_kernel<<<1, 1024, 0, st>>>(logical_counts, (int)E, R, n_red, phys_to_logical, phys_rank,
+                                           replica_count, logical_to_phys, 1 + n_red, rank_load);
+  return launch_status();
+}
+
 }  // namespace moe
 
 MOE_API size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P) {
@@ -341,4 +461,11 @@ MOE_API moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int3
                                   int32_t *logical_to_phys, moe_stream_t stream) {
   return moe::eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
                        logical_to_phys, moe::as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_redundant,
+                                           int32_t *phys_to_logical, int32_t *phys_rank, int32_t *replica_count,
+                                           int32_t *logical_to_phys, double *rank_load, moe_stream_t stream) {
+  return moe::eplb_balanced_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
+                                logical_to_phys, rank_load, moe::as_cuda(stream));
 }

@@ -50,10 +50,11 @@ class Layer:
     exposed through moe_layer_aux_t."""
 
     def __init__(self, T, d, E, k, I, R, act_dtype, expert_dtype, shared=False, n_redundant=0,
-                 weights: PackedWeights | None = None, keep_aux=True, device="cuda"):
+                 weights: PackedWeights | None = None, keep_aux=True, device="cuda", eplb_placement=0):
         s = Shape()
         s.T, s.d, s.E, s.I, s.k, s.R = T, d, E, I, k, R
         s.n_redundant, s.shared, s.act_dtype, s.expert_dtype = n_redundant, int(shared), act_dtype, expert_dtype
+        s.eplb_placement = eplb_placement
         self.shape, self.device = s, device
         self.weights = weights
         self.ws_bytes = moe_layer_workspace_size(s)
@@ -81,7 +82,7 @@ class Layer:
             b["phys_to_logical"] = torch.empty(P, **i32)
             b["phys_rank"] = torch.empty(P, **i32)
             b["replica_count"] = torch.empty(E, **i32)
-            b["logical_to_phys"] = torch.empty((E, 2), **i32)
+            b["logical_to_phys"] = torch.empty((E, 1 + n_redundant if eplb_placement == 1 else 2), **i32)
             self.aux = LayerAux(**{n: t.data_ptr() for n, t in b.items()})
 
     def forward(self, logits, x, out=None, stream=None):

@@ -78,12 +78,15 @@ typedef struct {
   float pad2_;
 } moe_load_stats_t;
 
-/* EPLB replica map (device arrays), as written by moe_eplb_map. */
+/* EPLB replica map (device arrays), as written by moe_eplb_map or
+ * moe_eplb_balanced_map. */
 typedef struct {
-  int32_t P;                      /* physical experts, E + n_redundant        */
-  const int32_t *phys_to_logical; /* [P]                                       */
-  const int32_t *replica_count;   /* [E], 1 or 2                               */
-  const int32_t *logical_to_phys; /* [E, 2]: primary, replica (-1 when none)   */
+  int32_t P;                      /* physical experts, E + n_redundant                  */
+  const int32_t *phys_to_logical; /* [P]                                                 */
+  const int32_t *replica_count;   /* [E], >= 1                                           */
+  const int32_t *logical_to_phys; /* [E, max_replicas]: replica j of expert e (-1 unused) */
+  int32_t max_replicas;           /* row length of logical_to_phys: 2 for moe_eplb_map,
+                                     1 + n_redundant for moe_eplb_balanced_map; 0 reads as 2 */
 } moe_eplb_t;
 
 /* Packed expert weights (produced by moe_pack_weights), one set per logical
@@ -114,10 +117,15 @@ typedef struct {
 typedef struct {
   int64_t T, d, E, I;
   int32_t k, R;
-  int32_t n_redundant;      /* EPLB replicas, 0 = off; must be a multiple of R and <= E */
+  int32_t n_redundant;      /* EPLB replicas, 0 = off; with eplb_placement 0 a multiple
+                               of R and <= E                                           */
   int32_t shared;           /* 1 = always-on shared expert (weight set E, weight 1)     */
   moe_dtype_t act_dtype;    /* x and out: MOE_F32 (with f32 experts) or MOE_BF16        */
   moe_dtype_t expert_dtype; /* MOE_F32, MOE_BF16 or MOE_E4M3                            */
+  int32_t eplb_placement;   /* with n_redundant > 0: 0 = one replica for each of the
+                               n_redundant hottest experts (moe_eplb_map); 1 = the
+                               load-aware placement (moe_eplb_balanced_map, needs only
+                               (E + n_redundant) % R == 0)                              */
 } moe_shape_t;
 
 /* Optional device buffers that receive the layer's intermediate results; any
@@ -136,7 +144,7 @@ typedef struct {
   int32_t *phys_to_logical; /* [P]      */
   int32_t *phys_rank;       /* [P]      */
   int32_t *replica_count;   /* [E]      */
-  int32_t *logical_to_phys; /* [E, 2]   */
+  int32_t *logical_to_phys; /* [E, 2], or [E, 1 + n_redundant] with eplb_placement 1 */
 } moe_layer_aux_t;
 
 /* Static text for a status code. */
@@ -201,13 +209,36 @@ moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int32_t R,
                           int32_t *phys_rank, int32_t *replica_count,
                           int32_t *logical_to_phys, moe_stream_t stream);
 
+/* Load-aware EPLB placement ("6.4 Data parallelism and expert parallelism",
+ * section 5.2, the placement with redundant slots that the page's simulation
+ * compares against the contiguous one).  logical_counts [E] int32.  In the page's
+ * order: each of the n_redundant extra slots goes to the expert whose load per
+ * replica (count / replicas) is highest, the lowest expert id on a tie; every
+ * replica of an expert carries count / replicas; the P = E + n_redundant replicas,
+ * heaviest first (equal loads keep expert then replica order), each go to the rank
+ * with the smallest load so far among those with one of their S = P / R slots
+ * free (the lowest rank on a tie) and take its next slot.  Physical id = rank * S +
+ * slot.  Outputs (device): phys_to_logical [P], phys_rank [P], replica_count [E],
+ * logical_to_phys [E, 1 + n_redundant] (replica j of expert e in placement order,
+ * -1 past replica_count[e]), rank_load [R] fp64 (optional, may be NULL).  Loads
+ * are fp64 quotients compared and summed in that order, so the map is exact.  Use it
+ * with moe_dispatch_layout through a moe_eplb_t with max_replicas = 1 + n_redundant.
+ * Requires E <= 1024, R <= 1024, P <= 2048, P % R == 0.  One CTA; for rebalancing,
+ * not for every step. */
+moe_status_t moe_eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t R,
+                                   int32_t n_redundant, int32_t *phys_to_logical,
+                                   int32_t *phys_rank, int32_t *replica_count,
+                                   int32_t *logical_to_phys, double *rank_load,
+                                   moe_stream_t stream);
+
 /* Bytes of workspace moe_dispatch_layout needs. */
 size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P);
 
 /* Dispatch layout ("6.4 ...", section 3.1, step 2 "Dispatch" and its figure:
  * each token is copied k times to the cards that own its experts; section 5.1:
  * busiest card / average).  topk_ids [T, k] int32 in [0, E).  Physical expert of
- * slot (t, j): e, or with `eplb` logical_to_phys[e][t mod replica_count[e]].
+ * slot (t, j): e, or with `eplb` logical_to_phys[e][t mod replica_count[e]] (rows of
+ * eplb->max_replicas entries).
  * Physical experts are numbered rank-major (linear placement, P/R per rank), so
  * rows sorted by physical expert are sorted by (rank, expert); inside an expert,
  * rows are in ascending token order.  Outputs (device, int32):

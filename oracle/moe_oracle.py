@@ -137,6 +137,57 @@ def greedy_rebalance(counts, R: int, n_redundant: int) -> np.ndarray:
     return np.array(load)
 
 
+def eplb_balanced_map(logical_counts, R: int, n_redundant: int) -> dict:
+    """The page's load-aware placement ("6.4 ...", section 5.2, the placement with
+    replicas) written out as a physical-expert map, in the map format of eplb_map.
+
+    Steps, in the page's order: each redundant slot goes to the expert whose load
+    per replica is highest (the first such expert on a tie); every replica of an
+    expert carries count / replicas; the replicas, heaviest first (equal loads keep
+    expert order, then replica order), each go to the lightest rank that still has
+    one of its S = (E + n_red) / R slots free (the lowest rank on a tie), taking that
+    rank's next slot.  Physical id = rank * S + slot; replica j of expert e is its
+    j-th replica in that order.  rank_load holds the per-rank loads the page prints
+    (greedy_rebalance gives the same numbers)."""
+    counts = [int(c) for c in np.asarray(logical_counts).ravel()]
+    E = len(counts)
+    P = E + n_redundant
+    if P % R:
+        raise ValueError("physical experts must divide evenly over ranks")
+    replicas = [1] * E
+    for _ in range(n_redundant):
+        best = 0
+        for i in range(1, E):
+            if counts[i] / replicas[i] > counts[best] / replicas[best]:
+                best = i
+        replicas[best] += 1
+    copies = []                                  # (load, expert, replica index)
+    for e in range(E):
+        for j in range(replicas[e]):
+            copies.append((counts[e] / replicas[e], e, j))
+    copies.sort(key=lambda c: -c[0])             # stable: ties keep expert, replica order
+    S = P // R
+    load = [0.0] * R
+    used = [0] * R
+    phys_to_logical = np.empty(P, dtype=np.int32)
+    phys_rank = np.empty(P, dtype=np.int32)
+    logical_to_phys = np.full((E, 1 + n_redundant), -1, dtype=np.int32)
+    for c, e, j in copies:
+        g = None
+        for r in range(R):
+            if used[r] < S and (g is None or load[r] < load[g]):
+                g = r
+        p = g * S + used[g]
+        load[g] += c
+        used[g] += 1
+        phys_to_logical[p] = e
+        phys_rank[p] = g
+        logical_to_phys[e, j] = p
+    return {"P": P, "phys_to_logical": phys_to_logical, "phys_rank": phys_rank,
+            "replica_count": np.array(replicas, dtype=np.int32), "logical_to_phys": logical_to_phys,
+            "rank_load": np.array(load)}
+
+
 # ============================================================== EPLB map
 def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int) -> dict:
     """One-step redundant-expert map ("6.4 ...", section 5.3; "How Expert
@@ -369,7 +420,8 @@ def _as64(a, kind):
 
 def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
     """The layer forward for a workload `cfg` (fields T, d, E, k, I, R, shared,
-    n_redundant, dtype).
+    n_redundant, dtype, and eplb_placement: 1 builds the EPLB map with
+    eplb_balanced_map instead of eplb_map).
 
     logits: float32 [T, E]; x: [T, d] float32 (fp32) or bf16 bits (uint16);
     weight(which, e) -> logical matrix (which in w_gate, w_up, w_down, ws_gate, ws_up,
@@ -383,7 +435,8 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
         eplb_enabled = cfg.n_redundant > 0
     emap = None
     if eplb_enabled:
-        emap = eplb_map(np.bincount(ids.ravel(), minlength=E), R, cfg.n_redundant)
+        build = eplb_balanced_map if getattr(cfg, "eplb_placement", 0) == 1 else eplb_map
+        emap = build(np.bincount(ids.ravel(), minlength=E), R, cfg.n_redundant)
     lay = dispatch_layout(ids, E, R, emap)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     xin = np.asarray(x)

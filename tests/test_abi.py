@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.LoadStats) == 32
     assert ctypes.sizeof(moe.Weights) == 64
-    assert ctypes.sizeof(moe.Shape) == 56
+    assert ctypes.sizeof(moe.Shape) == 64
     assert ctypes.sizeof(moe.LayerAux) == 14 * 8
 
 
@@ -53,6 +53,11 @@ def test_host_validation_without_gpu(lib):
     assert L.moe_route(None, 4, 2000, 2, None, None, None, None) == 1      # E > 1024
     assert L.moe_route(None, 0, 8, 2, None, None, None, None) == 0         # empty batch: nothing queued
     assert L.moe_eplb_map(None, 256, 32, 33, None, None, None, None, None) == 1  # n_red % R
+    assert L.moe_eplb_balanced_map(None, 256, 32, 33, None, None, None, None, None, None) == 1  # P % R
+    assert L.moe_eplb_balanced_map(None, 1025, 1, 0, None, None, None, None, None, None) == 1   # E > 1024
+    assert L.moe_eplb_balanced_map(None, 1024, 1, 1025, None, None, None, None, None, None) == 1  # P > 2048
+    fake4 = ctypes.c_void_p(256)
+    assert L.moe_eplb_balanced_map(fake4, 256, 8, 8, None, fake4, fake4, fake4, None, None) == 1  # null output
     assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0
     assert L.moe_combine(None, 1, None, None, 4, 2, 100, None, None, 1, None) == 1   # d % 8
     ws = L.moe_dispatch_workspace_size(64, 2, 8)

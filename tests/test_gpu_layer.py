@@ -33,7 +33,8 @@ def run_layer(cfg):
     ex = dtype_code(cfg.dtype)
     pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
     fill_weights(cfg, pw)
-    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw)
+    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw,
+                  eplb_placement=cfg.eplb_placement)
     logits = mi.make_logits(cfg)
     x = mi.make_x(cfg)
     out = layer.forward(dev_f32(logits), dev_x(cfg, x))
@@ -106,6 +107,11 @@ def test_layer_bf16_small_full():
 
 def test_layer_bf16_small_eplb_full():
     check(mi.config(3).scaled(T=200, d=256, E=16, I=256, R=4, n_redundant=4))
+
+
+def test_layer_bf16_small_balanced_eplb_full():
+    # the load-aware placement: the hottest experts take several replicas; P % R only
+    check(mi.config(3).scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1))
 
 
 def test_layer_decode_bf16():

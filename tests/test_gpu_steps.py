@@ -83,7 +83,7 @@ def gpu_layout(ids_np, E, R, eplb=None):
         rc = torch.from_numpy(eplb["replica_count"]).cuda()
         l2p = torch.from_numpy(eplb["logical_to_phys"]).cuda()
         keep = [p2l, rc, l2p]
-        ep = moe.Eplb(P, p2l.data_ptr(), rc.data_ptr(), l2p.data_ptr())
+        ep = moe.Eplb(P, p2l.data_ptr(), rc.data_ptr(), l2p.data_ptr(), eplb["logical_to_phys"].shape[1])
     moe.moe_dispatch_layout(ids, T, k, E, R, ep, out["lc"], out["pc"], out["po"], out["rc"], out["ro"], out["r2t"],
                             out["s2r"], stats, ws, wsb, err)
     torch.cuda.synchronize()
@@ -177,6 +177,57 @@ def test_eplb_map(E, R, n_red):
 def layout_for(cfg):
     ids, w = O.route(mi.make_logits(cfg), cfg.k)
     return ids, w, O.dispatch_layout(ids, cfg.E, cfg.R)
+
+
+def gpu_balanced_map(counts, R, n_red):
+    E = counts.size
+    P = E + n_red
+    c = torch.from_numpy(counts.astype(np.int32)).cuda()
+    p2l = torch.full((P,), -9, **I32)
+    prank = torch.full((P,), -9, **I32)
+    rc = torch.full((E,), -9, **I32)
+    l2p = torch.full((E, 1 + n_red), -9, **I32)
+    load = torch.full((R,), -1.0, dtype=torch.float64, device="cuda")
+    moe.moe_eplb_balanced_map(c, E, R, n_red, p2l, prank, rc, l2p, load)
+    torch.cuda.synchronize()
+    return {"phys_to_logical": p2l.cpu().numpy(), "phys_rank": prank.cpu().numpy(),
+            "replica_count": rc.cpu().numpy(), "logical_to_phys": l2p.cpu().numpy(),
+            "rank_load": load.cpu().numpy(), "P": P}
+
+
+@pytest.mark.parametrize("E,R,n_red,seed", [(256, 8, 0, 0), (256, 32, 32, 1), (256, 64, 64, 2), (256, 256, 256, 3),
+                                            (64, 4, 12, 4), (1024, 64, 1024, 5), (8, 3, 1, 6)])
+def test_eplb_balanced_map_exact(E, R, n_red, seed):
+    rng = np.random.default_rng(seed)
+    counts = rng.integers(0, 300, size=E)
+    counts[rng.integers(0, E, size=3)] = 5000        # hot experts that need several replicas
+    counts[:4] = counts[4]                           # ties, broken by expert id
+    g = gpu_balanced_map(counts, R, n_red)
+    r = O.eplb_balanced_map(counts, R, n_red)
+    for key in ("phys_to_logical", "phys_rank", "replica_count", "logical_to_phys"):
+        assert np.array_equal(g[key], r[key]), key
+    assert np.array_equal(g["rank_load"], r["rank_load"])   # fp64, same operations in the same order
+
+
+def test_eplb_balanced_map_page_simulation():
+    """The page's simulation counts through the GPU map: its printed busiest/average."""
+    import test_oracle_pins as pins
+    gold = pins.load("imbalance_sim_table.json")
+    counts = pins.page_simulation_counts(gold["setup"])
+    for row in gold["rows"]:
+        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
+            g = gpu_balanced_map(counts, row["ep"], n_red)
+            assert round(g["rank_load"].max() / g["rank_load"].mean(), 2) == row[col]
+
+
+@pytest.mark.parametrize("T,E,R,n_red", [(300, 16, 4, 4), (2048, 64, 8, 24), (8192, 256, 32, 32)])
+def test_layout_with_balanced_map(T, E, R, n_red):
+    rng = np.random.default_rng(T)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, : E // 8] += 2.0                        # a hot block of experts
+    ids, _ = O.route(logits, 4)
+    emap = O.eplb_balanced_map(np.bincount(ids.ravel(), minlength=E), R, n_red)
+    check_layout(ids, E, R, emap)
 
 
 @pytest.mark.parametrize("ci,T", [(0, None), (1, None), (2, 1024), (4, 512)])

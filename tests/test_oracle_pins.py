@@ -180,6 +180,56 @@ def test_sim_rebalance_columns(sim):
             assert round(load_.max() / load_.mean(), 2) == row[col]
 
 
+def test_balanced_map_reproduces_page_table(sim):
+    g, counts = sim
+    for row in g["rows"]:
+        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
+            m = O.eplb_balanced_map(counts, row["ep"], n_red)
+            assert round(m["rank_load"].max() / m["rank_load"].mean(), 2) == row[col]
+            assert np.array_equal(m["rank_load"], O.greedy_rebalance(counts, row["ep"], n_red))
+
+
+def test_balanced_map_worked_example():
+    # Worked by hand from the page's steps: counts 10, 6, 3, 1 over 2 ranks with 2
+    # redundant slots.  Slot 1 -> expert 0 (10 > 6), slot 2 -> expert 1 (6 > 5).
+    # Replicas, heaviest first: e0 5, e0 5, e1 3, e1 3, e2 3, e3 1; S = 3 slots per
+    # rank.  Ranks: e0 -> 0 (tie, lowest), e0 -> 1, e1 -> 0 (5 = 5), e1 -> 1,
+    # e2 -> 0 (8 = 8), e3 -> 1 (rank 0 is full).  Loads 11 and 9.
+    m = O.eplb_balanced_map(np.array([10, 6, 3, 1]), 2, 2)
+    assert m["replica_count"].tolist() == [2, 2, 1, 1]
+    assert m["phys_to_logical"].tolist() == [0, 1, 2, 0, 1, 3]
+    assert m["phys_rank"].tolist() == [0, 0, 0, 1, 1, 1]
+    assert m["logical_to_phys"].tolist() == [[0, 3, -1], [1, 4, -1], [2, -1, -1], [5, -1, -1]]
+    assert m["rank_load"].tolist() == [11.0, 9.0]
+
+
+def test_balanced_map_invariants():
+    rng = np.random.default_rng(11)
+    for E, R, n_red in ((256, 32, 32), (64, 8, 40), (30, 4, 10)):
+        counts = rng.integers(0, 1000, size=E)
+        counts[3] = 40000
+        m = O.eplb_balanced_map(counts, R, n_red)
+        P, S = E + n_red, (E + n_red) // R
+        assert np.bincount(m["phys_rank"], minlength=R).tolist() == [S] * R
+        assert m["replica_count"].sum() == P and m["replica_count"].min() >= 1
+        seen = np.zeros(P, dtype=bool)
+        for e in range(E):
+            row = m["logical_to_phys"][e]
+            n = m["replica_count"][e]
+            assert (row[n:] == -1).all() and (row[:n] >= 0).all()
+            assert (m["phys_to_logical"][row[:n]] == e).all() and not seen[row[:n]].any()
+            seen[row[:n]] = True
+            assert (row[:n] // S == m["phys_rank"][row[:n]]).all()
+        assert seen.all()
+        # the rank loads are the per-replica loads summed over each rank's slots
+        per = counts / m["replica_count"]
+        again = np.zeros(R)
+        np.add.at(again, m["phys_rank"], per[m["phys_to_logical"]])
+        assert np.allclose(again, m["rank_load"], rtol=1e-12, atol=0)
+        # the hottest expert (40000) holds the most replicas
+        assert m["replica_count"][3] == m["replica_count"].max()
+
+
 # ------------------------------------------------------------------ EPLB
 def test_eplb_map_geometry_and_hot_list():
     rng = np.random.default_rng(5)
