@@ -128,6 +128,12 @@ def _has_cuda():
     return torch.cuda.is_available()
 
 
+def job_throughput(world, tokens_per_rank, steps, max_ms):
+    """Whole-job tokens/s of weak scaling: every rank runs its own batch of
+    tokens_per_rank for `steps` steps, and the job takes as long as the slowest rank."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def dist_max(v):
     import torch
     import torch.distributed as dist
@@ -313,7 +319,7 @@ def run_ours(args, world, rank, local):
     per_stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)])
     total_ms = float(per_stage.sum())
     total_ms_max = dist_max(total_ms)
-    value = world * T * args.steps / (total_ms_max / 1e3)
+    value = job_throughput(world, T, args.steps, total_ms_max)
 
     # ---------------- roofline of the dominant kernel (the gate/up GEMM)
     pk = peaks()
