@@ -15,7 +15,7 @@ __all__ = [
     "MoeError", "lib", "library_path", "MOE_F32", "MOE_BF16", "MOE_E4M3",
     "MOE_DEV_NONFINITE_LOGIT", "MOE_DEV_ID_RANGE", "MOE_DEV_TIMEOUT", "MOE_DEV_LAYOUT",
     "LoadStats", "Eplb", "Weights", "Shape", "LayerAux",
-    "moe_status_string", "moe_route", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
+    "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
     "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error", "EXPORTED",
@@ -30,7 +30,7 @@ MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 << 20
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
 
-EXPORTED = ("moe_status_string", "moe_route", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
+EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
             "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error")
@@ -93,6 +93,7 @@ def lib():
             "moe_status_string": (ctypes.c_char_p, [st]),
             "moe_last_cuda_error": (ctypes.c_char_p, []),
             "moe_route": (st, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
+            "moe_route_biased": (st, [c_vp, c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_balanced_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
@@ -156,6 +157,11 @@ def moe_status_string(s: int) -> str:
 
 def moe_route(logits, T, E, k, topk_ids, topk_w, err=None, stream=None):
     _check("moe_route", lib().moe_route(_p(logits), T, E, k, _p(topk_ids), _p(topk_w), _p(err), _s(stream)))
+
+
+def moe_route_biased(logits, selection_bias, T, E, k, topk_ids, topk_w, err=None, stream=None):
+    _check("moe_route_biased", lib().moe_route_biased(_p(logits), _p(selection_bias), T, E, k, _p(topk_ids),
+                                                      _p(topk_w), _p(err), _s(stream)))
 
 
 def moe_eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count, logical_to_phys,

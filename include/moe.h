@@ -164,6 +164,17 @@ moe_status_t moe_route(const float *logits, int64_t T, int64_t E, int32_t k,
                        int32_t *topk_ids, float *topk_w, int32_t *err,
                        moe_stream_t stream);
 
+/* moe_route with a per-expert selection bias ("6.4 ...", section 5.1: the
+ * bias term that balances expert load without an auxiliary loss).  The experts are
+ * picked by logit + selection_bias[e] (fp32 sum; ties to the lower index), and their
+ * weights are the softmax of their unbiased logits renormalised over the k picked:
+ * w_j = exp(l_j - m) / sum_i exp(l_i - m), m the largest picked logit.
+ * selection_bias [E] fp32 (device) or NULL (= moe_route).  A non-finite logit or
+ * sum sets MOE_DEV_NONFINITE_LOGIT.  Limits as moe_route. */
+moe_status_t moe_route_biased(const float *logits, const float *selection_bias,
+                              int64_t T, int64_t E, int32_t k, int32_t *topk_ids,
+                              float *topk_w, int32_t *err, moe_stream_t stream);
+
 /* Size of the scratch array built into the library for moe_dispatch_layout_static. */
 #define MOE_DISPATCH_STATIC_SCRATCH_BYTES (4u << 20)
 

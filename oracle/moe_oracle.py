@@ -78,6 +78,28 @@ def route_softmax_then_renorm(logits: np.ndarray, k: int):
     return ids, sel / sel.sum(axis=1, keepdims=True)
 
 
+def route_selection_bias(logits: np.ndarray, bias: np.ndarray, k: int):
+    """Top-k routing with a selection bias ("6.4 ...", section 5.1: a bias term
+    instead of an auxiliary loss keeps expert counts even).  The experts are chosen
+    by the score logit + b_e, summed in float32 as the router's inputs are, ordered
+    (score descending, expert index ascending); the weights come from the unbiased
+    logits of the chosen experts: w_j = exp(l_j - m) / sum_i exp(l_i - m), m the
+    largest chosen logit, in float64.  bias = 0 gives route()."""
+    L = np.asarray(logits, dtype=np.float32)
+    b = np.asarray(bias, dtype=np.float32)
+    score = L + b[None, :]                       # float32 + float32 -> float32
+    if not (np.all(np.isfinite(L)) and np.all(np.isfinite(score))):
+        raise ValueError("non-finite router logit or score")
+    T, E = L.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    order = np.argsort(-score.astype(np.float64), axis=1, kind="stable")
+    ids = order[:, :k].astype(np.int32)
+    sel = np.take_along_axis(L.astype(np.float64), order[:, :k], axis=1)
+    e = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return ids, e / e.sum(axis=1, keepdims=True)
+
+
 # ============================================================== load statistics
 def rank_stats(rank_counts: np.ndarray, total_copies: int) -> dict:
     """Per-rank load ("Your expert-parallel deployment ...", "The three causes":

@@ -28,6 +28,27 @@ def gpu_route(logits, k, err=None):
     return ids.cpu().numpy(), w.cpu().numpy(), int(err.item())
 
 
+@pytest.mark.parametrize("T,E,k", [(129, 256, 8), (64, 8, 2), (1000, 64, 6), (33, 1024, 32)])
+def test_route_selection_bias(T, E, k):
+    rng = np.random.default_rng(T + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (0.5 * rng.standard_normal(E)).astype(np.float32)
+    bias[rng.integers(0, E)] = 3.0                   # an expert the bias pushes up
+    ids = torch.full((T, k), -7, **I32)
+    w = torch.full((T, k), -7.0, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, **I32)
+    moe.moe_route_biased(dev_f32(logits), dev_f32(bias), T, E, k, ids, w, err)
+    torch.cuda.synchronize()
+    rid, rw = O.route_selection_bias(logits, bias, k)
+    assert int(err.item()) == 0
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert close(w.cpu().numpy(), rw, F32_TOL)[0] == 0
+    # no bias: the plain router
+    moe.moe_route_biased(dev_f32(logits), None, T, E, k, ids, w, err)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), O.route(logits, k)[0])
+
+
 def check_route(logits, k):
     ids, w, err = gpu_route(logits, k)
     rid, rw = O.route(logits, k)

@@ -51,6 +51,41 @@ def test_route_brute_force_with_ties(E, k):
         assert abs(w.sum() - 1.0) < 1e-12
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (10, 4), (12, 3)])
+def test_route_selection_bias_brute_force(E, k):
+    rng = np.random.default_rng(E + k)
+    for trial in range(30):
+        l = rng.integers(-3, 4, size=(1, E)).astype(np.float32)
+        b = rng.integers(-2, 3, size=E).astype(np.float32)
+        ids, w = O.route_selection_bias(l, b, k)
+        score = (l[0] + b).tolist()
+        assert set(ids[0].tolist()) == brute_topk(score, k)      # picked by logit + bias
+        assert w.sum() == pytest.approx(1.0, abs=1e-15)
+        lv = l[0][ids[0]].astype(np.float64)                      # weighted by the logits alone
+        for a in range(k):
+            for c in range(k):
+                assert w[0, a] / w[0, c] == pytest.approx(np.exp(lv[a] - lv[c]), rel=1e-13)
+
+
+def test_route_selection_bias_special_cases():
+    rng = np.random.default_rng(3)
+    l = rng.standard_normal((32, 16)).astype(np.float32)
+    ids0, w0 = O.route(l, 4)
+    ids1, w1 = O.route_selection_bias(l, np.zeros(16), 4)
+    assert np.array_equal(ids0, ids1) and np.allclose(w0, w1, rtol=0, atol=1e-15)
+    b = np.zeros(16, dtype=np.float32)
+    b[5], b[9] = 1e4, -1e4              # always picked first / never picked
+    ids, w = O.route_selection_bias(l, b, 4)
+    assert (ids[:, 0] == 5).all() and not (ids == 9).any()
+    # the bias moves picks only: a token whose unbiased top-4 holds expert 5 and not 9
+    # keeps its experts and weights
+    keep = [t for t in range(32) if 5 in ids0[t] and 9 not in ids0[t]]
+    assert keep
+    for t in keep:
+        assert set(ids[t].tolist()) == set(ids0[t].tolist())
+        assert np.allclose(np.sort(w[t]), np.sort(w0[t]), rtol=0, atol=1e-15)
+
+
 def test_route_signed_zero_is_a_tie():
     l = np.array([[-0.0, 0.0, -1.0]], dtype=np.float32)
     ids, _ = O.route(l, 1)
