@@ -395,7 +395,7 @@ def run_ours(args, world, rank, local):
     e2e_ms = dist_max(sum(a.elapsed_time(b) for a, b in e_ev))
     if int(layer.err.item()) != 0:
         raise RuntimeError(f"device error word {int(layer.err.item())}")
-    e2e = {"value": round(world * T * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+    e2e = {"value": round(job_throughput(world, T, args.steps, e2e_ms), 1), "unit": UNIT,
            "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * h_x.element_size()),
            "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "api": "moe_layer_forward"}
 

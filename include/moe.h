@@ -298,8 +298,10 @@ size_t moe_ffn_workspace_size(int64_t rows, int64_t I, moe_dtype_t expert_dtype)
  * y bf16.  `rows_hint` is the number of routed rows N (phys_offsets[P] on the
  * device must equal it).  ws: moe_ffn_workspace_size(N + T_shared, I, dtype).
  * Limits (tensor-core paths): d % 128 == 0, I % 128 == 0, P <= 2048.  The tile
- * orientation follows the rows per expert; MOE_B300_FFN_TILES=swap|wide in the
- * environment forces one (both give the same results within rounding). */
+ * orientation follows the rows per expert (fewer than 64 rows per physical expert
+ * on average: weight rows x token rows; else SM-pair tiles of 256 token rows);
+ * MOE_B300_FFN_TILES=swap|wide|pair in the environment forces one (all give the
+ * same results within rounding). */
 moe_status_t moe_expert_ffn(const void *x_perm, const float *x_scales,
                             const int32_t *phys_offsets, int64_t P,
                             const int32_t *phys_to_logical, int64_t rows_hint,
