@@ -15,9 +15,13 @@
 //   wide  A = 128 token rows, B = weight rows (gate 128 + up 128, or 256 of
 //         W_down): one 128x256xK tile per feature block.  The one-SM form of the
 //         pair tiles (ffn_pair.cu) used for many rows per expert.
-//   swap  A = 128 weight rows (gate and up as two MMAs), B = up to 32 token rows:
-//         D is features x tokens, so a group of a few tokens streams its weights
-//         at HBM speed without padding tokens to 128.  For decode-sized batches.
+//   swap  A = 128 weight rows, B = up to 32 token rows: D is features x tokens, so a
+//         group of a few tokens streams its weights at HBM speed without padding
+//         tokens to 128.  For decode-sized batches.  Gate/up tiles hold 64 features:
+//         A rows 0-63 are W_gate^T, 64-127 W_up^T of the same features (two 8 KB
+//         copies of the packed block), so one MMA per K step gives gate in TMEM lanes
+//         0-63 and up in lanes 64-127; the up lanes' warps hand their values to the
+//         gate lanes' warps through shared memory (a bounded mbarrier each way).
 #include "grouped.cuh"
 
 namespace moe {
@@ -31,18 +35,20 @@ constexpr int kThreads = 192;
 
 template <bool kGated, bool kSwap, int kBW>
 struct Cfg {
-  static constexpr int kABytes = 128 * 128 * ((kSwap && kGated) ? 2 : 1);
+  static constexpr int kABytes = 128 * 128;
   static constexpr int kBRows = kSwap ? 32 : (kGated ? 256 : kBW);
   static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStage = kABytes + kBBytes;
-  static constexpr int kStages = kSwap ? (kGated ? 5 : 8) : 4;
-  static constexpr int kAccCols = kSwap ? (kGated ? 64 : 32) : (kGated ? 256 : kBW);
-  static constexpr int kTmemCols = kSwap ? (kGated ? 128 : 64) : (2 * kAccCols >= 512 ? 512 : 256);
+  static constexpr int kStages = kSwap ? 8 : 4;
+  static constexpr int kAccCols = kSwap ? 32 : (kGated ? 256 : kBW);
+  static constexpr int kTmemCols = kSwap ? 64 : (2 * kAccCols >= 512 ? 512 : 256);
   static constexpr int kTokTile = kSwap ? 32 : 128;
-  static constexpr int kFeatTile = kSwap ? 128 : (kGated ? 128 : kBW);
-  static constexpr int kBars = 2 * kStages + 5;
-  static constexpr size_t kSmem =
-      1024 + (size_t)kStages * kStage + kBars * 8 + 16 + (grouped::kMaxGroups + 1) * 4;
+  static constexpr int kFeatTile = kSwap ? (kGated ? 64 : 128) : (kGated ? 128 : kBW);
+  static constexpr bool kXchg = kSwap && kGated;  // up -> gate hand-off through shared memory
+  static constexpr int kXchgFloats = kXchg ? 2 * 64 * 33 : 0;  // [2 tiles][64 features][32 tokens + 1 pad]
+  static constexpr int kBars = 2 * kStages + 5 + (kXchg ? 4 : 0);
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kBars * 8 + 16 + (size_t)kXchgFloats * 4 +
+                                  (grouped::kMaxGroups + 1) * 4;
   static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -56,13 +62,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)C::kStages * C::kStage);
   int *misc = reinterpret_cast<int *>(bars + C::kBars);  // [0] TMEM base, [1] abort flag
-  int *tile_start = misc + 4;
+  float *xchg = reinterpret_cast<float *>(misc + 4);      // up values on their way to the gate lanes
+  int *tile_start = reinterpret_cast<int *>(xchg + C::kXchgFloats);
   const uint32_t stage0 = smem_u32(smem);
   auto full = [&](int s) { return smem_u32(&bars[s]); };
   auto empty = [&](int s) { return smem_u32(&bars[C::kStages + s]); };
   auto tfull = [&](int b) { return smem_u32(&bars[2 * C::kStages + b]); };
   auto tempty = [&](int b) { return smem_u32(&bars[2 * C::kStages + 2 + b]); };
   const uint32_t drain = smem_u32(&bars[2 * C::kStages + 4]);
+  auto xfull = [&](int b) { return smem_u32(&bars[2 * C::kStages + 5 + b]); };  // kXchg only
+  auto xfree = [&](int b) { return smem_u32(&bars[2 * C::kStages + 7 + b]); };
   uint16_t *out = static_cast<uint16_t *>(p.out);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -80,6 +89,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty(b), 128);
     }
     mbar_init(drain, 1);
+    if (C::kXchg)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(xfull(b), 64);
+        mbar_init(xfree(b), 64);
+      }
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -109,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb = kSwap ? (t.valid + 15) / 16 : 0;
       const uint32_t bytes = C::kABytes + (kSwap ? nb * 2048 : C::kBBytes);
       const int e = max(t.e, 0);
-      // gated: the gate+up block of this 128-feature block; down: the tile(s) of
-      // this block of output features
-      const int rt0 = kGated ? t.nt : t.nt * (C::kFeatTile / 128);
+      // gated: the gate+up block of this tile's 128-feature block (swap tiles take
+      // 64 of its features); down: the tile(s) of this block of output features
+      const int rt0 = kGated ? (kSwap ? t.nt >> 1 : t.nt) : t.nt * (C::kFeatTile / 128);
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
@@ -123,7 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kx = kb * 64;
         const uint32_t wdst = kSwap ? st : st + C::kABytes;
         auto wload = [&](uint32_t dst, const uint8_t *src, uint32_t n) { bulk_load(dst, src, n, bar); };
-        if (kGated) {
+        if (kGated && kSwap) {
+          // gate rows [64h, +64) and up rows [128 + 64h, +64) of the 256-row block
+          const uint8_t *blk = grouped::weight_block(p, e, rt0, kb, KB, grouped::kPairBytes);
+          const int h = t.nt & 1;
+          wload(wdst, blk + 8192 * h, 8192);
+          wload(wdst + 8192, blk + 16384 + 8192 * h, 8192);
+        } else if (kGated) {
           wload(wdst, grouped::weight_block(p, e, rt0, kb, KB, grouped::kPairBytes), grouped::kPairBytes);
         } else {
           wload(wdst, grouped::weight_block(p, e, rt0, kb, KB, grouped::kTileBytes), grouped::kTileBytes);
@@ -172,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (kb | kk) != 0;
           mma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id, acc);
-          if (kSwap && kGated) mma_bf16(d + 32, sdesc_sw128(a + 16384 + kk * 32), sdesc_sw128(bb + kk * 32), id, acc);
         }
         commit(empty(s));
         if (++s == C::kStages) {
@@ -225,21 +244,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
-      } else {
-        float v[32], u[32];
+      } else if (!kGated) {
+        float v[32];
         tmem_ld32(tb, v);
-        if (kGated) tmem_ld32(tb + 32, u);
         tmem_wait_ld();
         if (t.e >= 0) {
-          uint16_t *col = out + (int64_t)t.out_row * p.ld + (int64_t)t.nt * 128 + r;
+          uint16_t *col = out + (int64_t)t.out_row * p.ld + (int64_t)t.nt * C::kFeatTile + r;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c < t.valid) {
-              const float a = kGated ? silu(v[c]) * u[c] : v[c];
-              col[(int64_t)c * p.ld] = (uint16_t)f2bf(a);
-            }
-          }
+          for (int c = 0; c < 32; ++c)
+            if (c < t.valid) col[(int64_t)c * p.ld] = (uint16_t)f2bf(v[c]);
         }
+      } else {
+        // lanes 0-63: gate of feature r; lanes 64-127: up of feature r - 64
+        float v[32];
+        tmem_ld32(tb, v);
+        tmem_wait_ld();
+        fence_before();
+        mbar_arrive_relaxed(tempty(b));  // the accumulator is in registers
+        const int xb = it & 1, use = it >> 1;
+        float *xs = xchg + xb * 64 * 33;
+        if (q >= 2) {
+          // up lanes: pass the values on once the gate lanes have read the previous use
+          if (use > 0 && !mbar_wait(xfree(xb), (use - 1) & 1, abort_flag, p.err)) break;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) xs[(r - 64) * 33 + c] = v[c];
+          mbar_arrive(xfull(xb));
+        } else {
+          if (!mbar_wait(xfull(xb), use & 1, abort_flag, p.err)) break;
+          if (t.e >= 0) {
+            uint16_t *col = out + (int64_t)t.out_row * p.ld + (int64_t)t.nt * C::kFeatTile + r;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c < t.valid) col[(int64_t)c * p.ld] = (uint16_t)f2bf(silu(v[c]) * xs[r * 33 + c]);
+          }
+          mbar_arrive(xfree(xb));
+        }
+        continue;
       }
       fence_before();
       mbar_arrive_relaxed(tempty(b));
