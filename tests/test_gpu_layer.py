@@ -133,3 +133,48 @@ def test_layer_fp8_small_full():
 
 def test_layer_prefill_fp8_skew():
     check(mi.config(4), sample=sample_tokens(16384, n=3, seed=2))
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("decode-shaped bf16", dict(T=64, d=256, E=16, k=4, I=256, R=4)),
+    ("prefill-shaped bf16 with shared expert and EPLB", dict(T=600, d=512, E=8, k=2, I=256, R=4, shared=True,
+                                                            n_redundant=4, zipf_bias=True)),
+    ("fp8", dict(T=600, d=512, E=8, k=2, I=256, R=4, dtype="fp8", zipf_bias=True)),
+])
+def test_layer_forward_replays_in_a_cuda_graph(name, kw):
+    """moe_layer_forward queues work on the caller's stream only (no host syncs, no
+    allocation), so a CUDA graph captures it; replays on new inputs copied into the
+    captured buffers give exactly what eager calls give."""
+    cfg = mi.config(2).scaled(**{"shared": False, "zipf_bias": False, "dtype": "bf16", **kw})
+    act = moe.MOE_BF16
+    ex = dtype_code(cfg.dtype)
+    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
+    fill_weights(cfg, pw)
+    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw)
+    logits_in = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    x_in = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    batches = []
+    for seed in (1, 2, 3):
+        c = cfg.scaled(seed=seed)
+        batches.append((dev_f32(mi.make_logits(c)), dev_x(c, mi.make_x(c))))
+    eager = []
+    for lg, xx in batches:
+        eager.append(layer.forward(lg, xx).clone())
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):              # warm the launch paths outside the capture
+        logits_in.copy_(batches[0][0])
+        x_in.copy_(batches[0][1])
+        layer.forward(logits_in, x_in)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = layer.forward(logits_in, x_in)
+    for (lg, xx), ref in zip(batches, eager):
+        logits_in.copy_(lg)
+        x_in.copy_(xx)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(layer.err.item()) == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), name
