@@ -15,7 +15,8 @@ __all__ = [
     "MoeError", "lib", "library_path", "MOE_F32", "MOE_BF16", "MOE_E4M3",
     "MOE_DEV_NONFINITE_LOGIT", "MOE_DEV_ID_RANGE", "MOE_DEV_TIMEOUT", "MOE_DEV_LAYOUT",
     "LoadStats", "Eplb", "Weights", "Shape", "LayerAux",
-    "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
+    "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map",
+    "moe_eplb_window_update", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
     "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error", "EXPORTED",
@@ -30,7 +31,8 @@ MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 << 20
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
 
-EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map", "moe_dispatch_workspace_size",
+EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map",
+            "moe_eplb_window_update", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
             "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error")
@@ -96,6 +98,7 @@ def lib():
             "moe_route_biased": (st, [c_vp, c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_balanced_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+            "moe_eplb_window_update": (st, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
             "moe_dispatch_layout": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
                                     + [c_vp, sz, c_vp, c_vp]),
@@ -175,6 +178,11 @@ def moe_eplb_balanced_map(logical_counts, E, R, n_redundant, phys_to_logical, ph
     _check("moe_eplb_balanced_map",
            lib().moe_eplb_balanced_map(_p(logical_counts), E, R, n_redundant, _p(phys_to_logical), _p(phys_rank),
                                        _p(replica_count), _p(logical_to_phys), _p(rank_load), _s(stream)))
+
+
+def moe_eplb_window_update(logical_counts, window, W, E, step, window_sum, stream=None):
+    _check("moe_eplb_window_update", lib().moe_eplb_window_update(_p(logical_counts), _p(window), W, E, step,
+                                                                  _p(window_sum), _s(stream)))
 
 
 def moe_dispatch_workspace_size(T, k, P) -> int:

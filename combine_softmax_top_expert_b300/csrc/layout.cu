@@ -369,6 +369,18 @@ __global__ void __launch_bounds__(1024) eplb_balanced_kernel(const int32_t *__re
     for (int r = tid; r < R; r += blockDim.x) rank_load[r] = load[r];
 }
 
+// Sliding window of per-step logical expert counts ("6.4 ...", section 5.3: load
+// is averaged over window_size recent steps).  Thread e owns column e of the ring.
+__global__ void __launch_bounds__(256) eplb_window_kernel(const int32_t *__restrict__ counts, int32_t *ring,
+                                                          int64_t W, int E, int64_t step, int32_t *window_sum) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  ring[(step % W) * E + e] = counts[e];
+  int64_t sum = 0;
+  for (int64_t w = 0; w < W; ++w) sum += ring[w * E + e];
+  window_sum[e] = (int32_t)min(sum, (int64_t)INT32_MAX);
+}
+
 }  // namespace
 
 size_t dispatch_ws_bytes(int64_t T, int32_t k, int64_t P) {
@@ -468,4 +480,13 @@ MOE_API moe_status_t moe_eplb_balanced_map(const int32_t *logical_counts, int64_
                                            int32_t *logical_to_phys, double *rank_load, moe_stream_t stream) {
   return moe::eplb_balanced_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
                                 logical_to_phys, rank_load, moe::as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_eplb_window_update(const int32_t *logical_counts, int32_t *window, int64_t W, int64_t E,
+                                            int64_t step, int32_t *window_sum, moe_stream_t stream) {
+  if (W < 1 || W > (1 << 20) || E < 1 || E > 1024 || step < 0) return MOE_ERR_INVALID_ARG;
+  if (!logical_counts || !window || !window_sum) return MOE_ERR_INVALID_ARG;
+  moe::eplb_window_kernel<<<(unsigned)((E + 255) / 256), 256, 0, moe::as_cuda(stream)>>>(
+      logical_counts, window, W, (int)E, step, window_sum);
+  return moe::launch_status();
 }

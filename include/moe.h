@@ -242,6 +242,18 @@ moe_status_t moe_eplb_balanced_map(const int32_t *logical_counts, int64_t E, int
                                    int32_t *logical_to_phys, double *rank_load,
                                    moe_stream_t stream);
 
+/* EPLB's sliding window of loads ("6.4 Data parallelism and expert parallelism",
+ * section 5.3: the balancer averages per-expert load over window_size recent steps
+ * and rebalances every step_interval steps).  window [W, E] int32 is a ring the
+ * caller zero-fills once and keeps between calls; this call stores this step's
+ * logical_counts [E] (as moe_dispatch_layout writes them) in row step mod W and
+ * writes window_sum [E] = the sum over all W rows, i.e. over the last min(step + 1, W)
+ * steps (saturating at 2^31 - 1), ready for moe_eplb_balanced_map.  Requires
+ * 1 <= W <= 2^20, E <= 1024, step >= 0. */
+moe_status_t moe_eplb_window_update(const int32_t *logical_counts, int32_t *window,
+                                    int64_t W, int64_t E, int64_t step,
+                                    int32_t *window_sum, moe_stream_t stream);
+
 /* Bytes of workspace moe_dispatch_layout needs. */
 size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P);
 

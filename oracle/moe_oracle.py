@@ -210,6 +210,16 @@ def eplb_balanced_map(logical_counts, R: int, n_redundant: int) -> dict:
             "rank_load": np.array(load)}
 
 
+def eplb_window_sum(history, W: int) -> np.ndarray:
+    """EPLB's load window ("6.4 ...", section 5.3: per-expert load over window_size
+    recent steps): the per-expert sum of the last W per-step logical count vectors
+    (all of them while fewer than W have been seen)."""
+    h = [np.asarray(c, dtype=np.int64) for c in history]
+    if W < 1 or not h:
+        raise ValueError("need W >= 1 and at least one step")
+    return np.sum(h[-W:], axis=0)
+
+
 # ============================================================== EPLB map
 def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int) -> dict:
     """One-step redundant-expert map ("6.4 ...", section 5.3; "How Expert

@@ -56,6 +56,8 @@ def test_host_validation_without_gpu(lib):
     assert L.moe_eplb_balanced_map(None, 256, 32, 33, None, None, None, None, None, None) == 1  # P % R
     assert L.moe_eplb_balanced_map(None, 1025, 1, 0, None, None, None, None, None, None) == 1   # E > 1024
     assert L.moe_eplb_balanced_map(None, 1024, 1, 1025, None, None, None, None, None, None) == 1  # P > 2048
+    assert L.moe_eplb_window_update(None, None, 0, 8, 0, None, None) == 1      # W < 1
+    assert L.moe_eplb_window_update(None, None, 4, 2048, 0, None, None) == 1   # E > 1024
     fake4 = ctypes.c_void_p(256)
     assert L.moe_eplb_balanced_map(fake4, 256, 8, 8, None, fake4, fake4, fake4, None, None) == 1  # null output
     assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0

@@ -241,6 +241,28 @@ def test_eplb_balanced_map_page_simulation():
             assert round(g["rank_load"].max() / g["rank_load"].mean(), 2) == row[col]
 
 
+@pytest.mark.parametrize("W,E", [(3, 8), (1, 256), (5, 256)])
+def test_eplb_window_then_balanced_map(W, E):
+    """Per-step counts through the device ring; each step's window sum, and the
+    load-aware map built on it, equal the oracle's."""
+    rng = np.random.default_rng(W + E)
+    ring = torch.zeros((W, E), **I32)
+    wsum = torch.full((E,), -1, **I32)
+    history = []
+    for step in range(7):
+        counts = rng.integers(0, 500, size=E).astype(np.int32)
+        counts[step % E] += 3000                      # a hot expert that moves
+        history.append(counts)
+        moe.moe_eplb_window_update(torch.from_numpy(counts).cuda(), ring, W, E, step, wsum)
+        torch.cuda.synchronize()
+        ref = O.eplb_window_sum(history, W)
+        assert np.array_equal(wsum.cpu().numpy(), ref)
+    g = gpu_balanced_map(ref, 8, 8)
+    r = O.eplb_balanced_map(ref, 8, 8)
+    assert np.array_equal(g["logical_to_phys"], r["logical_to_phys"])
+    assert np.array_equal(g["rank_load"], r["rank_load"])
+
+
 @pytest.mark.parametrize("T,E,R,n_red", [(300, 16, 4, 4), (2048, 64, 8, 24), (8192, 256, 32, 32)])
 def test_layout_with_balanced_map(T, E, R, n_red):
     rng = np.random.default_rng(T)

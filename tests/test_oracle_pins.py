@@ -265,6 +265,14 @@ def test_balanced_map_invariants():
         assert m["replica_count"][3] == m["replica_count"].max()
 
 
+def test_eplb_window_sum_by_hand():
+    steps = [[1, 2], [3, 4], [5, 6], [7, 8]]
+    assert O.eplb_window_sum(steps[:1], 3).tolist() == [1, 2]            # fewer steps than W
+    assert O.eplb_window_sum(steps[:3], 3).tolist() == [9, 12]
+    assert O.eplb_window_sum(steps, 3).tolist() == [15, 18]              # the oldest step left
+    assert O.eplb_window_sum(steps, 1).tolist() == [7, 8]
+
+
 # ------------------------------------------------------------------ EPLB
 def test_eplb_map_geometry_and_hot_list():
     rng = np.random.default_rng(5)
