@@ -86,3 +86,29 @@ def test_layer_workspace_sizes(lib):
     s = moe.Shape()
     s.T, s.d, s.E, s.I, s.k, s.R, s.act_dtype, s.expert_dtype = 4, 128, 8, 64, 2, 4, moe.MOE_F32, moe.MOE_BF16
     assert moe.moe_layer_workspace_size(s) == 0    # fp32 activations need fp32 experts
+
+
+def test_empty_batch_and_unsupported_shapes_without_gpu(lib):
+    """Calls the library answers on the host, before any CUDA call."""
+    L = moe.lib()
+    fake = ctypes.c_void_p(256)
+    w = moe.Weights()
+    w.dtype, w.has_shared, w.E_w, w.d, w.I = moe.MOE_BF16, 0, 8, 256, 256
+    w.w13, w.w2 = 256, 256
+    s = moe.Shape()
+    s.T, s.d, s.E, s.I, s.k, s.R, s.act_dtype, s.expert_dtype = 0, 256, 8, 256, 2, 4, moe.MOE_BF16, moe.MOE_BF16
+    # an empty batch is a no-op
+    assert L.moe_layer_forward(ctypes.byref(s), None, None, ctypes.byref(w), None, None, None, 0, None, None) == 0
+    # an unknown EPLB placement is rejected
+    s.T, s.n_redundant, s.eplb_placement = 16, 4, 7
+    assert moe.moe_layer_workspace_size(s) == 0
+    # e4m3 experts need d % 256 == 0 (the pair tiles' 256 output features)
+    w8 = moe.Weights()
+    w8.dtype, w8.has_shared, w8.E_w, w8.d, w8.I = moe.MOE_E4M3, 0, 8, 384, 256
+    w8.w13 = w8.w2 = w8.s13 = w8.s2 = 256
+    ws = moe.moe_ffn_workspace_size(64, 256, moe.MOE_E4M3)
+    assert L.moe_expert_ffn(fake, fake, fake, 8, None, 64, ctypes.byref(w8), None, 0, fake, fake, ws, None,
+                            None) == 2
+    # the shared expert needs its weight set
+    assert L.moe_expert_ffn(fake, None, fake, 8, None, 64, ctypes.byref(w), fake, 16, fake, fake, 1 << 30, None,
+                            None) == 1

@@ -95,6 +95,15 @@ def test_device_generator_matches_host():
     assert np.array_equal(dev, mi.make_weight_host(cfg, "ws_up", 0))
 
 
+@pytest.mark.parametrize("kw", [dict(E=1, k=1, R=1), dict(E=8, k=8, R=4), dict(E=4, k=2, R=4, T=1)])
+def test_layer_bf16_degenerate_routing(kw):
+    # one expert takes every token (E = k = 1); every token takes every expert (k = E);
+    # a single token
+    base = dict(T=300, d=256, I=256, shared=False, zipf_bias=False)
+    base.update(kw)
+    check(mi.config(2).scaled(**base))
+
+
 # ------------------------------------------------------------------ bf16 workloads
 def sample_tokens(T, n=6, seed=0):
     rng = np.random.default_rng(seed)
