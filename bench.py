@@ -307,17 +307,38 @@ def run_ours(args, world, rank, local):
 
     props = torch.cuda.get_device_properties(dev)
     uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else None
+    # per-stage breakdown: the entry points one by one, events between them
     evs = [new_events() for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    per_stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)])
+
+    # the step itself: moe_layer_forward on inputs resident in HBM (one call, the same
+    # kernels without a Python round trip between launches)
+    layer = Layer(T, d, E, k, I, R, act, ex, cfg.shared, cfg.n_redundant, pw, keep_aux=False, device=dev,
+                  eplb_placement=cfg.eplb_placement)
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(logits, x)
+    torch.cuda.synchronize()
+    if int(layer.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(layer.err.item())}")
+    s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(uuid) as clk:
         for i in range(args.steps):
             flush.zero_()
-            step(evs[i])
+            s_ev[i][0].record(stream)
+            layer.forward(logits, x)
+            s_ev[i][1].record(stream)
         torch.cuda.synchronize()
     barrier()
-    per_stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)])
-    total_ms = float(per_stage.sum())
+    total_ms = float(sum(a.elapsed_time(b) for a, b in s_ev))
     total_ms_max = dist_max(total_ms)
     value = job_throughput(world, T, args.steps, total_ms_max)
 
@@ -365,8 +386,6 @@ def run_ours(args, world, rank, local):
                                  if roof["bound"] == "hbm" else "2*rows*d*2I flops")})
 
     # ---------------- end to end through moe_layer_forward, host buffers
-    layer = Layer(T, d, E, k, I, R, act, ex, cfg.shared, cfg.n_redundant, pw, keep_aux=False, device=dev,
-                  eplb_placement=cfg.eplb_placement)
     h_logits = torch.from_numpy(logits_np).pin_memory()
     h_x = (torch.from_numpy(x_np) if cfg.dtype == "fp32" else torch.from_numpy(x_np.view(np.int16))).pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
