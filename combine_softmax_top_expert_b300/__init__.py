@@ -19,7 +19,8 @@ __all__ = [
     "moe_eplb_window_update", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error", "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
+    "moe_selftest_wait_timeout", "EXPORTED",
     "MOE_DISPATCH_STATIC_SCRATCH_BYTES",
 ]
 
@@ -35,7 +36,8 @@ EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map"
             "moe_eplb_window_update", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error")
+            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
+            "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -99,6 +101,7 @@ def lib():
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_balanced_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_window_update": (st, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
+            "moe_selftest_wait_timeout": (st, [c_vp, c_i64, c_vp, c_vp]),
             "moe_dispatch_workspace_size": (sz, [c_i64, c_i32, c_i64]),
             "moe_dispatch_layout": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
                                     + [c_vp, sz, c_vp, c_vp]),
@@ -183,6 +186,13 @@ def moe_eplb_balanced_map(logical_counts, E, R, n_redundant, phys_to_logical, ph
 def moe_eplb_window_update(logical_counts, window, W, E, step, window_sum, stream=None):
     _check("moe_eplb_window_update", lib().moe_eplb_window_update(_p(logical_counts), _p(window), W, E, step,
                                                                   _p(window_sum), _s(stream)))
+
+
+def moe_selftest_wait_timeout(err, timeout_ns, waited_ms=None, stream=None):
+    """Run the kernels' bounded pipeline wait on a barrier nothing arrives on; it
+    must give up after timeout_ns and OR MOE_DEV_TIMEOUT into err."""
+    _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(_p(err), timeout_ns, _p(waited_ms),
+                                                                        _s(stream)))
 
 
 def moe_dispatch_workspace_size(T, k, P) -> int:

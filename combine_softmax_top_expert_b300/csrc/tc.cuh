@@ -74,7 +74,8 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, ui
 // and reports MOE_DEV_TIMEOUT.  Short waits poll (the fastest wake-up); after a
 // while the thread sleeps at most 0.5 ms at a time, looking at the flag and the
 // clock between sleeps.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
+                                          uint64_t timeout_ns = kTimeoutNs) {
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
     if (mbar_try(bar, parity)) return true;
@@ -82,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   for (;;) {
     if (mbar_try_sleep(bar, parity, 500000u)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kTimeoutNs) {
+    if (globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
       raise_dev(err, MOE_DEV_TIMEOUT);
       return false;

@@ -254,6 +254,16 @@ moe_status_t moe_eplb_window_update(const int32_t *logical_counts, int32_t *wind
                                     int64_t W, int64_t E, int64_t step,
                                     int32_t *window_sum, moe_stream_t stream);
 
+/* Self-test of the failure path shared by the tensor-core kernels (no counterpart
+ * on the pages): one thread runs their bounded pipeline wait on an mbarrier that
+ * nothing arrives on, with a limit of timeout_ns (1 us .. 100 ms) instead of the
+ * kernels' 2 s.  The wait gives up, ORs MOE_DEV_TIMEOUT into *err, writes the time
+ * it waited in ms to *waited_ms (may be NULL; -1 had it succeeded) and the kernel
+ * returns; the context stays usable.  A test and diagnostic aid, not part of the
+ * forward pass. */
+moe_status_t moe_selftest_wait_timeout(int32_t *err, int64_t timeout_ns, int32_t *waited_ms,
+                                       moe_stream_t stream);
+
 /* Bytes of workspace moe_dispatch_layout needs. */
 size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P);
 

@@ -60,6 +60,8 @@ def test_host_validation_without_gpu(lib):
     assert L.moe_eplb_window_update(None, None, 4, 2048, 0, None, None) == 1   # E > 1024
     fake4 = ctypes.c_void_p(256)
     assert L.moe_eplb_balanced_map(fake4, 256, 8, 8, None, fake4, fake4, fake4, None, None) == 1  # null output
+    assert L.moe_selftest_wait_timeout(None, 1000000, None, None) == 1          # no error word
+    assert L.moe_selftest_wait_timeout(fake4, 10**9, None, None) == 1          # limit above 100 ms
     assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0
     assert L.moe_combine(None, 1, None, None, 4, 2, 100, None, None, 1, None) == 1   # d % 8
     ws = L.moe_dispatch_workspace_size(64, 2, 8)
