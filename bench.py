@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=8, help="tokens in the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--override", action="append", default=[], metavar="FIELD=INT",
-                    help="change a shape field of the workload (T, E, R, k, d, I), e.g. for a small profiling case")
+                    help="change an integer field of the workload (T, E, R, k, d, I, n_redundant, eplb_placement, "
+                         "expert_placement), e.g. for a small profiling case")
     return ap.parse_args()
 
 
@@ -104,6 +105,7 @@ def workload_config(cfg):
     return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "R": cfg.R,
             "shared_expert": cfg.shared, "redundant_experts": cfg.n_redundant, "experts_dtype": cfg.dtype,
             "eplb_placement": ("load-aware" if cfg.eplb_placement else "hottest experts") if cfg.n_redundant else None,
+            "expert_placement": "round-robin" if cfg.expert_placement == 1 else "linear",
             "l2": "flushed between timed steps (512 MiB write)", "parallelism": "independent batch per GPU"}
 
 
@@ -258,13 +260,15 @@ def run_ours(args, world, rank, local):
     y = torch.empty((rows, d), dtype=torch.float32 if act == moe.MOE_F32 else torch.bfloat16, device=dev)
     out = torch.empty((T, d), dtype=y.dtype, device=dev)
     err = torch.zeros(1, **i32)
-    eplb = moe.Eplb(P, p2l.data_ptr(), repc.data_ptr(), l2p.data_ptr(), reps) if cfg.n_redundant else None
+    rr = cfg.expert_placement == 1
+    mapped = cfg.n_redundant > 0 or rr      # physical ids differ from the logical ones
+    eplb = moe.Eplb(P, p2l.data_ptr(), repc.data_ptr(), l2p.data_ptr(), reps, int(rr)) if mapped else None
     y_dt = moe.MOE_F32 if act == moe.MOE_F32 else moe.MOE_BF16
     perm_dt = ex if ex == moe.MOE_E4M3 else act
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stage_names = ["route", "dispatch_layout", "permute", "expert_gate_up", "expert_down", "combine"]
-    launches = {"route": 1, "dispatch_layout": 3 * (2 if cfg.n_redundant else 1) + (1 if cfg.n_redundant else 0),
+    launches = {"route": 1, "dispatch_layout": 3 * (2 if cfg.n_redundant else 1) + (1 if mapped else 0),
                 "permute": 1, "expert_gate_up": 1, "expert_down": 1, "combine": 1}
 
     def step(ev):
@@ -276,15 +280,17 @@ def run_ours(args, world, rank, local):
             if balanced:
                 moe.moe_eplb_balanced_map(lc, E, R, cfg.n_redundant, p2l, prank, repc, l2p)
             else:
-                moe.moe_eplb_map(lc, E, R, cfg.n_redundant, p2l, prank, repc, l2p)
+                moe.moe_placement_map(lc, E, R, cfg.n_redundant, int(rr), p2l, prank, repc, l2p)
+        elif rr:
+            moe.moe_placement_map(None, E, R, 0, 1, p2l, prank, repc, l2p)
         moe.moe_dispatch_layout(ids, T, k, E, R, eplb, lc, pc, po, rc, ro, r2t, s2r, stats, dws, dws_b, err)
         ev[2].record(stream)
         moe.moe_permute(x, act, T, d, k, s2r, xp, perm_dt, xs)
         ev[3].record(stream)
-        moe.moe_expert_gate_up(xp, xs, po, P, p2l if cfg.n_redundant else None, N, W, x if cfg.shared else None,
+        moe.moe_expert_gate_up(xp, xs, po, P, p2l if mapped else None, N, W, x if cfg.shared else None,
                                T_sh, h, hs, err)
         ev[4].record(stream)
-        moe.moe_expert_down(h, hs, po, P, p2l if cfg.n_redundant else None, N, W, T_sh, y, err)
+        moe.moe_expert_down(h, hs, po, P, p2l if mapped else None, N, W, T_sh, y, err)
         ev[5].record(stream)
         moe.moe_combine(y, y_dt, s2r, tw, T, k, d, y[N:] if cfg.shared else None, out, act)
         ev[6].record(stream)
@@ -321,7 +327,7 @@ def run_ours(args, world, rank, local):
     # the step itself: moe_layer_forward on inputs resident in HBM (one call, the same
     # kernels without a Python round trip between launches)
     layer = Layer(T, d, E, k, I, R, act, ex, cfg.shared, cfg.n_redundant, pw, keep_aux=False, device=dev,
-                  eplb_placement=cfg.eplb_placement)
+                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement)
     for _ in range(max(args.warmup, 3)):
         layer.forward(logits, x)
     torch.cuda.synchronize()

@@ -15,8 +15,8 @@ __all__ = [
     "MoeError", "lib", "library_path", "MOE_F32", "MOE_BF16", "MOE_E4M3",
     "MOE_DEV_NONFINITE_LOGIT", "MOE_DEV_ID_RANGE", "MOE_DEV_TIMEOUT", "MOE_DEV_LAYOUT",
     "LoadStats", "Eplb", "Weights", "Shape", "LayerAux",
-    "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map",
-    "moe_eplb_window_update", "moe_dispatch_workspace_size",
+    "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_placement_map",
+    "moe_eplb_balanced_map", "moe_eplb_window_update", "moe_dispatch_workspace_size",
     "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
     "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
@@ -32,7 +32,8 @@ MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 << 20
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
 
-EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_eplb_balanced_map",
+EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_placement_map",
+            "moe_eplb_balanced_map",
             "moe_eplb_window_update", "moe_dispatch_workspace_size",
             "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
@@ -57,7 +58,7 @@ class LoadStats(ctypes.Structure):
 
 class Eplb(ctypes.Structure):
     _fields_ = [("P", c_i32), ("phys_to_logical", c_vp), ("replica_count", c_vp), ("logical_to_phys", c_vp),
-                ("max_replicas", c_i32)]
+                ("max_replicas", c_i32), ("base_placement", c_i32)]
 
 
 class Weights(ctypes.Structure):
@@ -68,7 +69,7 @@ class Weights(ctypes.Structure):
 class Shape(ctypes.Structure):
     _fields_ = [("T", c_i64), ("d", c_i64), ("E", c_i64), ("I", c_i64), ("k", c_i32), ("R", c_i32),
                 ("n_redundant", c_i32), ("shared", c_i32), ("act_dtype", c_i32), ("expert_dtype", c_i32),
-                ("eplb_placement", c_i32)]
+                ("eplb_placement", c_i32), ("expert_placement", c_i32)]
 
 
 class LayerAux(ctypes.Structure):
@@ -78,6 +79,7 @@ class LayerAux(ctypes.Structure):
 
 
 assert ctypes.sizeof(LoadStats) == 32 and ctypes.sizeof(Weights) == 64 and ctypes.sizeof(Shape) == 64
+assert ctypes.sizeof(Eplb) == 40
 
 # ------------------------------------------------------------------ loading
 _lib = None
@@ -99,6 +101,7 @@ def lib():
             "moe_route": (st, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_route_biased": (st, [c_vp, c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+            "moe_placement_map": (st, [c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_balanced_map": (st, [c_vp, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_eplb_window_update": (st, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
             "moe_selftest_wait_timeout": (st, [c_vp, c_i64, c_vp, c_vp]),
@@ -168,6 +171,13 @@ def moe_route(logits, T, E, k, topk_ids, topk_w, err=None, stream=None):
 def moe_route_biased(logits, selection_bias, T, E, k, topk_ids, topk_w, err=None, stream=None):
     _check("moe_route_biased", lib().moe_route_biased(_p(logits), _p(selection_bias), T, E, k, _p(topk_ids),
                                                       _p(topk_w), _p(err), _s(stream)))
+
+
+def moe_placement_map(logical_counts, E, R, n_redundant, placement, phys_to_logical, phys_rank, replica_count,
+                      logical_to_phys, stream=None):
+    _check("moe_placement_map", lib().moe_placement_map(_p(logical_counts), E, R, n_redundant, placement,
+                                                        _p(phys_to_logical), _p(phys_rank), _p(replica_count),
+                                                        _p(logical_to_phys), _s(stream)))
 
 
 def moe_eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count, logical_to_phys,

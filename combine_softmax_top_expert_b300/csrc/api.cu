@@ -12,6 +12,8 @@ moe_status_t dispatch_layout(const int32_t *, int64_t, int32_t, int64_t, int32_t
                              void *, size_t, int32_t *, cudaStream_t);
 moe_status_t eplb_balanced_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *,
                                int32_t *, double *, cudaStream_t);
+moe_status_t placement_map(const int32_t *, int64_t, int32_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *,
+                           int32_t *, cudaStream_t);
 moe_status_t eplb_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *, int32_t *,
                       cudaStream_t);
 moe_status_t permute(const void *, moe_dtype_t, int64_t, int64_t, int32_t, const int32_t *, void *, moe_dtype_t,
@@ -97,7 +99,7 @@ struct LayerPlan {
   int64_t T, N, P, d, I, E;
   int32_t k, R;
   size_t act_bytes, perm_bytes, y_bytes;
-  bool eplb, shared, balanced;
+  bool eplb, shared, balanced, round_robin, mapped;
   // byte offsets into the workspace
   size_t o_ids, o_w, o_lc, o_pc, o_po, o_rc, o_ro, o_r2t, o_s2r, o_stats, o_p2l, o_prank, o_repc, o_l2p, o_disp,
       o_xp, o_xs, o_y, o_ffn, total;
@@ -118,6 +120,9 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
   p->eplb = s->n_redundant > 0;
   if (s->eplb_placement != 0 && s->eplb_placement != 1) return false;
   p->balanced = p->eplb && s->eplb_placement == 1;
+  if (s->expert_placement != 0 && s->expert_placement != 1) return false;
+  p->round_robin = s->expert_placement == 1;
+  p->mapped = p->eplb || p->round_robin;  // physical ids differ from logical ones
   p->shared = s->shared != 0;
   p->P = s->E + s->n_redundant;
   p->act_bytes = s->act_dtype == MOE_F32 ? 4 : 2;
@@ -262,23 +267,27 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
 
   moe_status_t r;
   if ((r = moe_route(logits, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK) return r;
-  moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p, p.balanced ? (int32_t)(1 + p.P - p.E) : 2};
+  moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p, p.balanced ? (int32_t)(1 + p.P - p.E) : 2, p.round_robin ? 1 : 0};
   if (p.eplb) {
     // counts of this batch's logical routing, then the replica map built on them
     if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, nullptr, lc, pc, po, rc, ro, r2t, s2r, stats, disp,
                              disp_bytes, err, st)) != MOE_OK)
       return r;
     r = p.balanced ? eplb_balanced_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p2l, prank, repc, l2p, nullptr, st)
-                   : eplb_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p2l, prank, repc, l2p, st);
+                   : placement_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p.round_robin ? 1 : 0, p2l, prank, repc,
+                                   l2p, st);
     if (r != MOE_OK) return r;
+  } else if (p.round_robin) {
+    // no replicas: the map only renumbers the experts rank-major
+    if ((r = placement_map(nullptr, p.E, p.R, 0, 1, p2l, prank, repc, l2p, st)) != MOE_OK) return r;
   }
-  if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.eplb ? &map : nullptr, lc, pc, po, rc, ro, r2t, s2r, stats,
+  if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.mapped ? &map : nullptr, lc, pc, po, rc, ro, r2t, s2r, stats,
                            disp, disp_bytes, err, st)) != MOE_OK)
     return r;
   const moe_dtype_t perm_dt = s->expert_dtype == MOE_E4M3 ? MOE_E4M3 : s->act_dtype;
   if ((r = permute(x, s->act_dtype, p.T, p.d, p.k, s2r, xp, perm_dt, xs, st)) != MOE_OK) return r;
   const int64_t T_sh = p.shared ? p.T : 0;
-  if ((r = expert_ffn(xp, xs, po, p.P, p.eplb ? p2l : nullptr, p.N, w, p.shared ? x : nullptr, T_sh, y, fws,
+  if ((r = expert_ffn(xp, xs, po, p.P, p.mapped ? p2l : nullptr, p.N, w, p.shared ? x : nullptr, T_sh, y, fws,
                       ffn_ws_bytes(p.N + T_sh, p.I, s->expert_dtype), err, st)) != MOE_OK)
     return r;
   const moe_dtype_t y_dt = s->expert_dtype == MOE_F32 ? MOE_F32 : MOE_BF16;

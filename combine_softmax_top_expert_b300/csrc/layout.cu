@@ -18,7 +18,11 @@
 //
 // EPLB map ("6.4 ...", section 5.3; "How Expert Parallelism Works for
 // Mixture-of-Experts Models in vLLM", "MoE Layer Construction"): one CTA ranks the
-// experts by (count desc, index asc) and writes the physical tables.
+// experts by (count desc, index asc) and writes the physical tables.  The base
+// slots follow the placement strategy ("How Expert Parallelism Works ...",
+// "Configuring Expert Parallelism", linear or round_robin): linear puts logical
+// expert e on rank e / (E/R), round-robin on rank e % R, in local slot e % (E/R)
+// or e / R.
 #include "common.cuh"
 
 namespace moe {
@@ -97,14 +101,16 @@ struct StatsOut {
   moe_load_stats_t *stats;  // [2]
 };
 
-// Warp-level statistics of `counts` [n] grouped into R ranks of n/R entries.
-__device__ void warp_stats(const int32_t *counts, int n, int R, int64_t total, moe_load_stats_t *out) {
+// Warp-level statistics of `counts` [n] grouped into R ranks of n/R entries: rank r
+// holds entries r*(n/R) .. (linear) or r, r + R, r + 2R, .. (round-robin).
+__device__ void warp_stats(const int32_t *counts, int n, int R, int64_t total, bool round_robin,
+                           moe_load_stats_t *out) {
   const int lane = threadIdx.x & 31;
   const int per = n / R;
   int max_rank = 0, max_exp = 0, active = 0;
   for (int r = lane; r < R; r += 32) {
     int s = 0;
-    for (int i = 0; i < per; ++i) s += counts[r * per + i];
+    for (int i = 0; i < per; ++i) s += counts[round_robin ? r + i * R : r * per + i];
     max_rank = max(max_rank, s);
   }
   for (int i = lane; i < n; i += 32) {
@@ -132,7 +138,7 @@ __device__ void warp_stats(const int32_t *counts, int n, int R, int64_t total, m
 }
 
 __global__ void __launch_bounds__(1024) layout_scan_kernel(int32_t *__restrict__ hist, int chunks, int P, int E,
-                                                           int R, int64_t N, const int32_t *p2l,
+                                                           int R, int64_t N, const int32_t *p2l, bool base_rr,
                                                            int32_t *logical_counts, int32_t *phys_counts,
                                                            int32_t *phys_offsets, int32_t *rank_counts,
                                                            int32_t *rank_offsets, moe_load_stats_t *stats) {
@@ -210,8 +216,9 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(int32_t *__restrict__
     if (lane == 0) rank_offsets[R] = run;
   }
   if (stats) {
-    if (warp == 1) warp_stats(lcnt, E, R, N, &stats[0]);
-    if (warp == 2) warp_stats(cnt, P, R, N, &stats[1]);
+    // before: the logical experts in their base placement; after: the physical ones
+    if (warp == 1) warp_stats(lcnt, E, R, N, base_rr, &stats[0]);
+    if (warp == 2) warp_stats(cnt, P, R, N, false, &stats[1]);
   }
 }
 
@@ -234,20 +241,27 @@ __global__ void __launch_bounds__(256) layout_scatter_kernel(const int32_t *__re
   row_to_token[row] = (int32_t)(s / m.k);
 }
 
+// counts may be null when n_red == 0 (no hot list to rank).
 __global__ void __launch_bounds__(1024) eplb_map_kernel(const int32_t *__restrict__ counts, int E, int R, int n_red,
-                                                        int32_t *phys_to_logical, int32_t *phys_rank,
-                                                        int32_t *replica_count, int32_t *logical_to_phys) {
+                                                        bool round_robin, int32_t *phys_to_logical,
+                                                        int32_t *phys_rank, int32_t *replica_count,
+                                                        int32_t *logical_to_phys) {
   __shared__ int32_t c[1024];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = counts[e];
+  if (n_red > 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = counts[e];
   __syncthreads();
   const int base = E / R, S = (E + n_red) / R;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int ce = c[e];
-    int rank = 0;
-    for (int f = 0; f < E; ++f) rank += (c[f] > ce) || (c[f] == ce && f < e);
-    const int pr = (e / base) * S + e % base;
+    int rank = n_red;  // position in the hot list; n_red = not hot
+    if (n_red > 0) {
+      const int ce = c[e];
+      rank = 0;
+      for (int f = 0; f < E; ++f) rank += (c[f] > ce) || (c[f] == ce && f < e);
+    }
+    const int home = round_robin ? e % R : e / base, slot0 = round_robin ? e / R : e % base;
+    const int pr = home * S + slot0;
     phys_to_logical[pr] = e;
-    phys_rank[pr] = e / base;
+    phys_rank[pr] = home;
     logical_to_phys[2 * e] = pr;
     if (rank < n_red) {
       const int r = rank % R, slot = base + rank / R;
@@ -401,6 +415,7 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
     return MOE_ERR_INVALID_ARG;
   if (eplb && (!eplb->phys_to_logical || !eplb->replica_count || !eplb->logical_to_phys))
     return MOE_ERR_INVALID_ARG;
+  if (eplb && eplb->base_placement != 0 && eplb->base_placement != 1) return MOE_ERR_INVALID_ARG;
   const int64_t N = T * k;
   if (N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if (N > 0 && (!topk_ids || !row_to_token || !slot_to_row)) return MOE_ERR_INVALID_ARG;
@@ -421,7 +436,8 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
     layout_count_kernel<<<chunks, 256, smem, st>>>(topk_ids, N, (int)P, m, hist, chunk_rank, err);
   }
   layout_scan_kernel<<<1, 1024, 0, st>>>(hist, chunks, (int)P, (int)E, R, N,
-                                         eplb ? eplb->phys_to_logical : nullptr, logical_counts, phys_counts,
+                                         eplb ? eplb->phys_to_logical : nullptr,
+                                         eplb != nullptr && eplb->base_placement == 1, logical_counts, phys_counts,
                                          phys_offsets, rank_counts, rank_offsets, stats);
   if (N > 0)
     layout_scatter_kernel<<<(unsigned)((N + 255) / 256), 256, 0, st>>>(topk_ids, N, (int)P, m, hist, chunk_rank,
@@ -429,14 +445,23 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
   return launch_status();
 }
 
+moe_status_t placement_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_red, int32_t placement,
+                           int32_t *phys_to_logical, int32_t *phys_rank, int32_t *replica_count,
+                           int32_t *logical_to_phys, cudaStream_t st) {
+  if (E < 1 || E > 1024 || R < 1 || E % R || n_red < 0 || n_red % R || n_red > E) return MOE_ERR_INVALID_ARG;
+  if (placement != 0 && placement != 1) return MOE_ERR_INVALID_ARG;
+  if ((n_red > 0 && !logical_counts) || !phys_to_logical || !phys_rank || !replica_count || !logical_to_phys)
+    return MOE_ERR_INVALID_ARG;
+  eplb_map_kernel<<<1, 1024, 0, st>>>(logical_counts, (int)E, R, n_red, placement == 1, phys_to_logical, phys_rank,
+                                      replica_count, logical_to_phys);
+  return launch_status();
+}
+
 moe_status_t eplb_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_red, int32_t *phys_to_logical,
                       int32_t *phys_rank, int32_t *replica_count, int32_t *logical_to_phys, cudaStream_t st) {
-  if (E < 1 || E > 1024 || R < 1 || E % R || n_red < 0 || n_red % R || n_red > E) return MOE_ERR_INVALID_ARG;
-  if (!logical_counts || !phys_to_logical || !phys_rank || !replica_count || !logical_to_phys)
-    return MOE_ERR_INVALID_ARG;
-  eplb_map_kernel<<<1, 1024, 0, st>>>(logical_counts, (int)E, R, n_red, phys_to_logical, phys_rank, replica_count,
-                                      logical_to_phys);
-  return launch_status();
+  if (!logical_counts) return MOE_ERR_INVALID_ARG;
+  return placement_map(logical_counts, E, R, n_red, 0, phys_to_logical, phys_rank, replica_count, logical_to_phys,
+                       st);
 }
 
 moe_status_t eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_red,
@@ -473,6 +498,13 @@ MOE_API moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int3
                                   int32_t *logical_to_phys, moe_stream_t stream) {
   return moe::eplb_map(logical_counts, E, R, n_redundant, phys_to_logical, phys_rank, replica_count,
                        logical_to_phys, moe::as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_placement_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_redundant,
+                                       int32_t placement, int32_t *phys_to_logical, int32_t *phys_rank,
+                                       int32_t *replica_count, int32_t *logical_to_phys, moe_stream_t stream) {
+  return moe::placement_map(logical_counts, E, R, n_redundant, placement, phys_to_logical, phys_rank, replica_count,
+                            logical_to_phys, moe::as_cuda(stream));
 }
 
 MOE_API moe_status_t moe_eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t R, int32_t n_redundant,

@@ -50,11 +50,12 @@ class Layer:
     exposed through moe_layer_aux_t."""
 
     def __init__(self, T, d, E, k, I, R, act_dtype, expert_dtype, shared=False, n_redundant=0,
-                 weights: PackedWeights | None = None, keep_aux=True, device="cuda", eplb_placement=0):
+                 weights: PackedWeights | None = None, keep_aux=True, device="cuda", eplb_placement=0,
+                 expert_placement=0):
         s = Shape()
         s.T, s.d, s.E, s.I, s.k, s.R = T, d, E, I, k, R
         s.n_redundant, s.shared, s.act_dtype, s.expert_dtype = n_redundant, int(shared), act_dtype, expert_dtype
-        s.eplb_placement = eplb_placement
+        s.eplb_placement, s.expert_placement = eplb_placement, expert_placement
         self.shape, self.device = s, device
         self.weights = weights
         self.ws_bytes = moe_layer_workspace_size(s)

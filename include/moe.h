@@ -85,8 +85,12 @@ typedef struct {
   const int32_t *phys_to_logical; /* [P]                                                 */
   const int32_t *replica_count;   /* [E], >= 1                                           */
   const int32_t *logical_to_phys; /* [E, max_replicas]: replica j of expert e (-1 unused) */
-  int32_t max_replicas;           /* row length of logical_to_phys: 2 for moe_eplb_map,
-                                     1 + n_redundant for moe_eplb_balanced_map; 0 reads as 2 */
+  int32_t max_replicas;           /* row length of logical_to_phys: 2 for moe_eplb_map and
+                                     moe_placement_map, 1 + n_redundant for
+                                     moe_eplb_balanced_map; 0 reads as 2 */
+  int32_t base_placement;         /* placement of the logical experts before replication,
+                                     for stats[0] of moe_dispatch_layout: 0 = linear
+                                     (rank e / (E/R)), 1 = round-robin (rank e % R) */
 } moe_eplb_t;
 
 /* Packed expert weights (produced by moe_pack_weights), one set per logical
@@ -123,9 +127,15 @@ typedef struct {
   moe_dtype_t act_dtype;    /* x and out: MOE_F32 (with f32 experts) or MOE_BF16        */
   moe_dtype_t expert_dtype; /* MOE_F32, MOE_BF16 or MOE_E4M3                            */
   int32_t eplb_placement;   /* with n_redundant > 0: 0 = one replica for each of the
-                               n_redundant hottest experts (moe_eplb_map); 1 = the
+                               n_redundant hottest experts (moe_placement_map); 1 = the
                                load-aware placement (moe_eplb_balanced_map, needs only
                                (E + n_redundant) % R == 0)                              */
+  int32_t expert_placement; /* base placement of the logical experts over the R ranks:
+                               0 = linear (rank e / (E/R)), 1 = round-robin (rank e % R).
+                               Sets the base slots of moe_placement_map and the "before"
+                               statistics; the load-aware map places every expert
+                               itself, so with eplb_placement 1 only the statistics
+                               change                                                   */
 } moe_shape_t;
 
 /* Optional device buffers that receive the layer's intermediate results; any
@@ -220,6 +230,21 @@ moe_status_t moe_eplb_map(const int32_t *logical_counts, int64_t E, int32_t R,
                           int32_t *phys_rank, int32_t *replica_count,
                           int32_t *logical_to_phys, moe_stream_t stream);
 
+/* moe_eplb_map with a choice of base placement ("How Expert Parallelism Works for
+ * Mixture-of-Experts Models in vLLM", "Configuring Expert Parallelism": the
+ * placement strategy is "linear" or "round_robin").  placement 0 = linear, as
+ * moe_eplb_map; 1 = round-robin: logical expert e sits on rank e % R in slot e / R
+ * (physical id (e % R) * S + e / R).  Replicas are placed as in moe_eplb_map.
+ * With n_redundant == 0 the map is the bare placement (P = E, every
+ * replica_count 1, logical_to_phys[e][1] = -1) and logical_counts may be NULL.
+ * Same outputs and limits as moe_eplb_map; a placement other than 0 or 1 is
+ * MOE_ERR_INVALID_ARG. */
+moe_status_t moe_placement_map(const int32_t *logical_counts, int64_t E, int32_t R,
+                               int32_t n_redundant, int32_t placement,
+                               int32_t *phys_to_logical, int32_t *phys_rank,
+                               int32_t *replica_count, int32_t *logical_to_phys,
+                               moe_stream_t stream);
+
 /* Load-aware EPLB placement ("6.4 Data parallelism and expert parallelism",
  * section 5.2, the placement with redundant slots that the page's simulation
  * compares against the contiguous one).  logical_counts [E] int32.  In the page's
@@ -272,16 +297,17 @@ size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P);
  * busiest card / average).  topk_ids [T, k] int32 in [0, E).  Physical expert of
  * slot (t, j): e, or with `eplb` logical_to_phys[e][t mod replica_count[e]] (rows of
  * eplb->max_replicas entries).
- * Physical experts are numbered rank-major (linear placement, P/R per rank), so
- * rows sorted by physical expert are sorted by (rank, expert); inside an expert,
- * rows are in ascending token order.  Outputs (device, int32):
+ * Physical experts are numbered rank-major (P/R per rank), so rows sorted by
+ * physical expert are sorted by (rank, expert); inside an expert, rows are in
+ * ascending token order.  Outputs (device, int32):
  *   logical_counts [E], phys_counts [P], phys_offsets [P+1] (exclusive scan),
  *   rank_counts [R], rank_offsets [R+1], row_to_token [N], slot_to_row [T, k];
- *   stats [2] (moe_load_stats_t): [0] logical experts over R ranks linearly
- *   (before replication), [1] the physical layout (after; equal to [0] without EPLB).
+ *   stats [2] (moe_load_stats_t): [0] logical experts over R ranks in the base
+ *   placement (eplb->base_placement; linear without eplb), before replication;
+ *   [1] the physical layout (after; equal to [0] when the map only renumbers).
  * ws: moe_dispatch_workspace_size(T, k, P) bytes, 256-byte aligned.
  * Ids out of range set MOE_DEV_ID_RANGE; those slots are left out of the layout.
- * Limits: P <= 2048, P % R == 0, E % R == 0. */
+ * Limits: P <= 2048, P % R == 0, E % R == 0, eplb->base_placement 0 or 1. */
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k,
                                  int64_t E, int32_t R, const moe_eplb_t *eplb,
                                  int32_t *logical_counts, int32_t *phys_counts,

@@ -18,7 +18,7 @@ Sources (page title, then the section the step follows):
   why.", "The three causes": compare max rank load against mean rank load.
 * "How Expert Parallelism Works for Mixture-of-Experts Models in vLLM", "MoE Layer
   Construction": num_physical_experts = num_experts + num_redundant_experts.
-* same page, "Configuring Expert Parallelism": "linear" placement.
+* same page, "Configuring Expert Parallelism": "linear" or "round_robin" placement.
 
 Readings where the pages are silent (each one is listed with its reason in the
 design notes): selection is on the fp32 logits, ties go to the lower expert index,
@@ -26,6 +26,7 @@ design notes): selection is on the fp32 logits, ties go to the lower expert inde
 SwiGLU is silu(x W_gate) * (x W_up) then W_down; rows are ordered by physical
 expert, then by token; EPLB replicas go to the n_red hottest experts (count desc,
 index asc), replica j to rank j mod R, token t uses replica t mod replica_count;
+round-robin placement puts expert e on rank e mod R in local slot e div R;
 the shared expert has weight 1 and is not renormalised; bf16 workloads round h and
 y to bf16 where the kernels store them; fp8 workloads quantise x and h per token per
 128-channel group and the weights per 128x128 block with scale = amax/448 (fp32)
@@ -127,6 +128,24 @@ def linear_rank_counts(expert_counts: np.ndarray, R: int) -> np.ndarray:
     return c.reshape(R, c.size // R).sum(axis=1)
 
 
+def round_robin_rank_counts(expert_counts: np.ndarray, R: int) -> np.ndarray:
+    """Round-robin placement: rank r owns experts r, r + R, r + 2R, ... ("How Expert
+    Parallelism Works ...", "Configuring Expert Parallelism", "round_robin"; the page
+    names the strategy only, so experts are dealt to the ranks in index order)."""
+    c = np.asarray(expert_counts, dtype=np.int64)
+    if c.size % R:
+        raise ValueError("experts must divide evenly over ranks")
+    return np.array([c[r::R].sum() for r in range(R)], dtype=np.int64)
+
+
+def base_rank_counts(expert_counts: np.ndarray, R: int, placement: str = "linear") -> np.ndarray:
+    if placement == "linear":
+        return linear_rank_counts(expert_counts, R)
+    if placement == "round_robin":
+        return round_robin_rank_counts(expert_counts, R)
+    raise ValueError(f"unknown placement {placement!r}")
+
+
 def greedy_rebalance(counts, R: int, n_redundant: int) -> np.ndarray:
     """The page's load-aware placement ("6.4 ...", section 5.2): hand each redundant
     slot to the expert with the highest load per replica (first such expert on a
@@ -221,19 +240,24 @@ def eplb_window_sum(history, W: int) -> np.ndarray:
 
 
 # ============================================================== EPLB map
-def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int) -> dict:
+def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int, placement: str = "linear") -> dict:
     """One-step redundant-expert map ("6.4 ...", section 5.3; "How Expert
-    Parallelism Works ...", "MoE Layer Construction").
+    Parallelism Works ...", "MoE Layer Construction" and "Configuring Expert
+    Parallelism" for the placement strategy).
 
     P = E + n_red physical experts, S = P / R per rank.  Rank r holds, in its slots
-    0 .. E/R-1, logical experts r*E/R + slot (its linear block), then replicas.
+    0 .. E/R-1, its base experts, then replicas: linear placement gives rank r the
+    logical experts r*E/R + slot, round-robin the experts r + slot*R.
     The n_red hottest logical experts (count desc, index asc) get one replica each;
     the j-th hottest goes to rank j mod R, slot E/R + j div R.  Physical id = r*S + slot.
+    With n_red = 0 this is the bare placement (the counts are not used).
     """
     c = np.asarray(logical_counts, dtype=np.int64)
     E = c.size
     if E % R or n_redundant % R or n_redundant > E:
         raise ValueError("unsupported EPLB geometry")
+    if placement not in ("linear", "round_robin"):
+        raise ValueError(f"unknown placement {placement!r}")
     P = E + n_redundant
     S, base = P // R, E // R
     hot = np.argsort(-c, kind="stable")[:n_redundant]
@@ -243,7 +267,7 @@ def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int) -> dict:
     replica_count = np.ones(E, dtype=np.int32)
     for r in range(R):
         for s in range(base):
-            e = r * base + s
+            e = r * base + s if placement == "linear" else r + s * R
             p = r * S + s
             phys_to_logical[p] = e
             phys_rank[p] = r
@@ -261,7 +285,8 @@ def eplb_map(logical_counts: np.ndarray, R: int, n_redundant: int) -> dict:
 
 
 # ============================================================== dispatch layout
-def dispatch_layout(topk_ids: np.ndarray, E: int, R: int, eplb: dict | None = None) -> dict:
+def dispatch_layout(topk_ids: np.ndarray, E: int, R: int, eplb: dict | None = None,
+                    placement: str = "linear") -> dict:
     """Counting, scan and the EP-rank-ordered layout ("6.4 ...", section 3.1 step 2
     Dispatch: each token is copied k times to the cards owning its experts; the
     figure's per-card copy counts).
@@ -269,7 +294,8 @@ def dispatch_layout(topk_ids: np.ndarray, E: int, R: int, eplb: dict | None = No
     Physical id of slot (t, j): the logical id e, or with EPLB
     logical_to_phys[e][t mod replica_count[e]].  Physical ids are numbered
     rank-major, so ordering rows by physical id orders them by (rank, expert);
-    inside an expert, rows are in ascending token order.
+    inside an expert, rows are in ascending token order.  The "before" statistics
+    count the logical experts on the ranks of the base `placement`.
     """
     ids = np.asarray(topk_ids, dtype=np.int64)
     T, k = ids.shape
@@ -294,7 +320,7 @@ def dispatch_layout(topk_ids: np.ndarray, E: int, R: int, eplb: dict | None = No
     phys_offsets = np.concatenate([[0], np.cumsum(phys_counts)]).astype(np.int64)
     rank_counts = linear_rank_counts(phys_counts, R)
     rank_offsets = np.concatenate([[0], np.cumsum(rank_counts)]).astype(np.int64)
-    before = rank_stats(linear_rank_counts(logical_counts, R), N)
+    before = rank_stats(base_rank_counts(logical_counts, R, placement), N)
     after = rank_stats(rank_counts, N)
     for st, cnt in ((before, logical_counts), (after, phys_counts)):
         st["max_expert"] = int(cnt.max()) if cnt.size else 0
@@ -452,8 +478,9 @@ def _as64(a, kind):
 
 def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
     """The layer forward for a workload `cfg` (fields T, d, E, k, I, R, shared,
-    n_redundant, dtype, and eplb_placement: 1 builds the EPLB map with
-    eplb_balanced_map instead of eplb_map).
+    n_redundant, dtype, eplb_placement: 1 builds the EPLB map with
+    eplb_balanced_map instead of eplb_map, and expert_placement: 1 places the
+    logical experts round-robin instead of linearly).
 
     logits: float32 [T, E]; x: [T, d] float32 (fp32) or bf16 bits (uint16);
     weight(which, e) -> logical matrix (which in w_gate, w_up, w_down, ws_gate, ws_up,
@@ -465,11 +492,16 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
     ids, w = route(logits, k)
     if eplb_enabled is None:
         eplb_enabled = cfg.n_redundant > 0
+    placement = "round_robin" if getattr(cfg, "expert_placement", 0) == 1 else "linear"
     emap = None
-    if eplb_enabled:
-        build = eplb_balanced_map if getattr(cfg, "eplb_placement", 0) == 1 else eplb_map
-        emap = build(np.bincount(ids.ravel(), minlength=E), R, cfg.n_redundant)
-    lay = dispatch_layout(ids, E, R, emap)
+    counts = np.bincount(ids.ravel(), minlength=E)
+    if eplb_enabled and getattr(cfg, "eplb_placement", 0) == 1:
+        emap = eplb_balanced_map(counts, R, cfg.n_redundant)
+    elif eplb_enabled:
+        emap = eplb_map(counts, R, cfg.n_redundant, placement)
+    elif placement == "round_robin":
+        emap = eplb_map(counts, R, 0, placement)
+    lay = dispatch_layout(ids, E, R, emap, placement)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     xin = np.asarray(x)
     kind = "fp32" if cfg.dtype == "fp32" else "bf16"

@@ -36,6 +36,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.LoadStats) == 32
     assert ctypes.sizeof(moe.Weights) == 64
     assert ctypes.sizeof(moe.Shape) == 64
+    assert ctypes.sizeof(moe.Eplb) == 40
     assert ctypes.sizeof(moe.LayerAux) == 14 * 8
 
 
@@ -60,6 +61,9 @@ def test_host_validation_without_gpu(lib):
     assert L.moe_eplb_window_update(None, None, 4, 2048, 0, None, None) == 1   # E > 1024
     fake4 = ctypes.c_void_p(256)
     assert L.moe_eplb_balanced_map(fake4, 256, 8, 8, None, fake4, fake4, fake4, None, None) == 1  # null output
+    assert L.moe_placement_map(fake4, 256, 32, 32, 2, fake4, fake4, fake4, fake4, None) == 1  # placement 2
+    assert L.moe_placement_map(None, 256, 32, 32, 1, fake4, fake4, fake4, fake4, None) == 1   # hot list, no counts
+    assert L.moe_placement_map(None, 256, 30, 0, 1, fake4, fake4, fake4, fake4, None) == 1    # E % R
     assert L.moe_selftest_wait_timeout(None, 1000000, None, None) == 1          # no error word
     assert L.moe_selftest_wait_timeout(fake4, 10**9, None, None) == 1          # limit above 100 ms
     assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0
@@ -101,9 +105,13 @@ def test_empty_batch_and_unsupported_shapes_without_gpu(lib):
     s.T, s.d, s.E, s.I, s.k, s.R, s.act_dtype, s.expert_dtype = 0, 256, 8, 256, 2, 4, moe.MOE_BF16, moe.MOE_BF16
     # an empty batch is a no-op
     assert L.moe_layer_forward(ctypes.byref(s), None, None, ctypes.byref(w), None, None, None, 0, None, None) == 0
-    # an unknown EPLB placement is rejected
+    # an unknown EPLB placement or base placement is rejected
     s.T, s.n_redundant, s.eplb_placement = 16, 4, 7
     assert moe.moe_layer_workspace_size(s) == 0
+    s.eplb_placement, s.expert_placement = 0, 2
+    assert moe.moe_layer_workspace_size(s) == 0
+    s.expert_placement = 1
+    assert moe.moe_layer_workspace_size(s) > 0
     # e4m3 experts need d % 256 == 0 (the pair tiles' 256 output features)
     w8 = moe.Weights()
     w8.dtype, w8.has_shared, w8.E_w, w8.d, w8.I = moe.MOE_E4M3, 0, 8, 384, 256

@@ -34,7 +34,7 @@ def run_layer(cfg):
     pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
     fill_weights(cfg, pw)
     layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw,
-                  eplb_placement=cfg.eplb_placement)
+                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement)
     logits = mi.make_logits(cfg)
     x = mi.make_x(cfg)
     out = layer.forward(dev_f32(logits), dev_x(cfg, x))
@@ -55,7 +55,7 @@ def check(cfg, sample=None):
     assert np.array_equal(b["rank_counts"], lay["rank_counts"])
     assert np.array_equal(b["row_to_token"], lay["row_to_token"])
     assert np.array_equal(b["slot_to_row"], lay["slot_to_row"])
-    if cfg.n_redundant:
+    if ref["eplb"] is not None:
         em = ref["eplb"]
         assert np.array_equal(b["phys_to_logical"], em["phys_to_logical"])
         assert np.array_equal(b["replica_count"], em["replica_count"])
@@ -121,6 +121,13 @@ def test_layer_bf16_small_eplb_full():
 def test_layer_bf16_small_balanced_eplb_full():
     # the load-aware placement: the hottest experts take several replicas; P % R only
     check(mi.config(3).scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(n_redundant=4), dict(n_redundant=8, eplb_placement=1)])
+def test_layer_bf16_small_round_robin(kw):
+    # round-robin base placement: alone (the map only renumbers), with hot-list
+    # replicas, and with the load-aware map (only the "before" statistics change)
+    check(mi.config(3).scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=0, expert_placement=1, **kw))
 
 
 def test_layer_decode_bf16():

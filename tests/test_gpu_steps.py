@@ -85,7 +85,7 @@ def test_route_flags_non_finite():
 
 
 # ------------------------------------------------------------------ layout / EPLB
-def gpu_layout(ids_np, E, R, eplb=None):
+def gpu_layout(ids_np, E, R, eplb=None, placement="linear"):
     T, k = ids_np.shape
     P = E if eplb is None else eplb["P"]
     N = T * k
@@ -104,7 +104,8 @@ def gpu_layout(ids_np, E, R, eplb=None):
         rc = torch.from_numpy(eplb["replica_count"]).cuda()
         l2p = torch.from_numpy(eplb["logical_to_phys"]).cuda()
         keep = [p2l, rc, l2p]
-        ep = moe.Eplb(P, p2l.data_ptr(), rc.data_ptr(), l2p.data_ptr(), eplb["logical_to_phys"].shape[1])
+        ep = moe.Eplb(P, p2l.data_ptr(), rc.data_ptr(), l2p.data_ptr(), eplb["logical_to_phys"].shape[1],
+                      1 if placement == "round_robin" else 0)
     moe.moe_dispatch_layout(ids, T, k, E, R, ep, out["lc"], out["pc"], out["po"], out["rc"], out["ro"], out["r2t"],
                             out["s2r"], stats, ws, wsb, err)
     torch.cuda.synchronize()
@@ -116,11 +117,11 @@ def gpu_layout(ids_np, E, R, eplb=None):
     return res
 
 
-def check_layout(ids, E, R, eplb=None):
+def check_layout(ids, E, R, eplb=None, placement="linear"):
     T, k = ids.shape
     N = T * k
-    g = gpu_layout(ids, E, R, eplb)
-    r = O.dispatch_layout(ids, E, R, eplb)
+    g = gpu_layout(ids, E, R, eplb, placement)
+    r = O.dispatch_layout(ids, E, R, eplb, placement)
     assert g["err"] == 0
     assert np.array_equal(g["lc"], r["logical_counts"])
     assert np.array_equal(g["pc"], r["phys_counts"])
@@ -192,6 +193,43 @@ def test_eplb_map(E, R, n_red):
     assert np.array_equal(prank.cpu().numpy(), ref["phys_rank"])
     assert np.array_equal(rc.cpu().numpy(), ref["replica_count"])
     assert np.array_equal(l2p.cpu().numpy(), ref["logical_to_phys"])
+
+
+@pytest.mark.parametrize("E,R,n_red", [(8, 4, 0), (8, 4, 4), (256, 32, 0), (256, 32, 32), (1024, 8, 8), (12, 3, 6)])
+def test_placement_map_round_robin(E, R, n_red):
+    rng = np.random.default_rng(E * 7 + R)
+    counts = rng.integers(0, 20, size=E).astype(np.int32)
+    ref = O.eplb_map(counts, R, n_red, "round_robin")
+    P = E + n_red
+    c = torch.from_numpy(counts).cuda() if n_red else None       # the bare placement reads no counts
+    p2l, prank = torch.full((P,), -9, **I32), torch.full((P,), -9, **I32)
+    rc, l2p = torch.full((E,), -9, **I32), torch.full((E, 2), -9, **I32)
+    moe.moe_placement_map(c, E, R, n_red, 1, p2l, prank, rc, l2p)
+    torch.cuda.synchronize()
+    assert np.array_equal(p2l.cpu().numpy(), ref["phys_to_logical"])
+    assert np.array_equal(prank.cpu().numpy(), ref["phys_rank"])
+    assert np.array_equal(rc.cpu().numpy(), ref["replica_count"])
+    assert np.array_equal(l2p.cpu().numpy(), ref["logical_to_phys"])
+    # placement 0 is moe_eplb_map
+    if n_red:
+        lin = O.eplb_map(counts, R, n_red)
+        moe.moe_placement_map(c, E, R, n_red, 0, p2l, prank, rc, l2p)
+        torch.cuda.synchronize()
+        assert np.array_equal(p2l.cpu().numpy(), lin["phys_to_logical"])
+        assert np.array_equal(l2p.cpu().numpy(), lin["logical_to_phys"])
+
+
+@pytest.mark.parametrize("T,E,R,n_red", [(64, 8, 4, 0), (777, 64, 8, 16), (4096, 256, 32, 0), (4096, 256, 32, 32)])
+def test_layout_round_robin(T, E, R, n_red):
+    rng = np.random.default_rng(T + 1)
+    l = rng.standard_normal((T, E)).astype(np.float32) + np.linspace(3, 0, E, dtype=np.float32)
+    ids, _ = O.route(l, 4)
+    emap = O.eplb_map(np.bincount(ids.ravel(), minlength=E), R, n_red, "round_robin")
+    check_layout(ids, E, R, emap, "round_robin")
+    # the load-aware map with round-robin "before" statistics
+    if n_red:
+        check_layout(ids, E, R, O.eplb_balanced_map(np.bincount(ids.ravel(), minlength=E), R, n_red),
+                     "round_robin")
 
 
 # ------------------------------------------------------------------ permute / combine

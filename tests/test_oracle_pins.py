@@ -316,6 +316,76 @@ def test_eplb_token_split_by_parity():
     assert np.array_equal(lay["slot_to_row"], s2r)
 
 
+def test_round_robin_placement_by_hand():
+    """8 experts on 4 ranks, one copy per token: round-robin deals experts 0..7 to
+    ranks 0,1,2,3,0,1,2,3; the busiest rank is worked out by hand."""
+    counts = [10, 0, 3, 5, 2, 7, 1, 4]
+    ids = np.repeat(np.arange(8), counts).astype(np.int32)[:, None]
+    lay = O.dispatch_layout(ids, 8, 4, O.eplb_map(np.zeros(8), 4, 0, "round_robin"), "round_robin")
+    # rank 0: e0 + e4 = 12; rank 1: e1 + e5 = 7; rank 2: e2 + e6 = 4; rank 3: e3 + e7 = 9
+    assert lay["rank_counts"].tolist() == [12, 7, 4, 9]
+    assert lay["stats_before"]["max_rank"] == 12 and lay["stats_after"]["max_rank"] == 12
+    assert lay["stats_before"]["max_over_mean"] == 1.5
+    # the linear placement of the same counts: 10, 8, 9, 5
+    lin = O.dispatch_layout(ids, 8, 4)
+    assert lin["rank_counts"].tolist() == [10, 8, 9, 5] and lin["stats_before"]["max_over_mean"] == 1.25
+
+
+@pytest.mark.parametrize("E,R,n_red", [(256, 32, 0), (256, 32, 32), (64, 8, 16), (12, 3, 6)])
+def test_round_robin_map_geometry(E, R, n_red):
+    rng = np.random.default_rng(E + n_red)
+    counts = rng.integers(0, 40, size=E)
+    m = O.eplb_map(counts, R, n_red, "round_robin")
+    lin = O.eplb_map(counts, R, n_red)
+    S = (E + n_red) // R
+    for e in range(E):
+        p = m["logical_to_phys"][e, 0]
+        assert p == (e % R) * S + e // R                  # rank e mod R, local slot e div R
+        assert m["phys_rank"][p] == e % R and m["phys_to_logical"][p] == e
+    assert np.bincount(m["phys_rank"], minlength=R).tolist() == [S] * R
+    assert sorted(m["phys_to_logical"][m["phys_rank"] == 0].tolist()[:E // R]) == list(range(0, E, R))
+    # replicas do not depend on the base placement
+    assert np.array_equal(m["hot"], lin["hot"])
+    for e in m["hot"]:
+        assert m["logical_to_phys"][e, 1] == lin["logical_to_phys"][e, 1]
+    assert np.array_equal(m["replica_count"], lin["replica_count"])
+
+
+@pytest.mark.parametrize("E,R", [(8, 1), (8, 8), (256, 256)])
+def test_round_robin_equals_linear_when_degenerate(E, R):
+    """One rank, or one expert per rank: both strategies give every rank the same experts."""
+    counts = np.arange(E)[::-1]
+    a, b = O.eplb_map(counts, R, 0, "round_robin"), O.eplb_map(counts, R, 0)
+    for key in ("phys_to_logical", "phys_rank", "logical_to_phys"):
+        assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("T,E,k,R", [(3, 8, 2, 4), (200, 16, 4, 8), (257, 32, 8, 4)])
+def test_round_robin_layout_brute_force(T, E, k, R):
+    """Rows in order (rank e mod R, slot e div R, token), straight from the rule."""
+    l = np.random.default_rng(T * E).standard_normal((T, E)).astype(np.float32)
+    ids, _ = O.route(l, k)
+    lay = O.dispatch_layout(ids, E, R, O.eplb_map(np.zeros(E), R, 0, "round_robin"), "round_robin")
+    r2t, s2r = brute_layout(ids, E, lambda t, e: (e % R) * (E // R) + e // R)
+    assert lay["row_to_token"].tolist() == r2t
+    assert np.array_equal(lay["slot_to_row"], s2r)
+    per_rank = [sum(1 for t in range(T) for j in range(k) if ids[t, j] % R == r) for r in range(R)]
+    assert lay["rank_counts"].tolist() == per_rank
+    assert lay["stats_before"]["max_rank"] == max(per_rank)
+
+
+def test_round_robin_layer_output_equals_linear():
+    """The placement moves rows between ranks; the layer's result is unchanged."""
+    cfg = mi.config(0)
+    l = mi.make_logits(cfg)
+    x = np.random.default_rng(3).standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    wt = tiny_weights(cfg, 4)
+    a = O.layer_forward(cfg, l, x, wt)
+    b = O.layer_forward(cfg.scaled(expert_placement=1), l, x, wt)
+    assert np.array_equal(a["out"], b["out"])
+    assert not np.array_equal(a["layout"]["row_to_token"], b["layout"]["row_to_token"])
+
+
 # ------------------------------------------------------------------ number formats
 def test_bf16_rounding_matches_torch():
     v = np.random.default_rng(3).standard_normal(100000) * 10.0
@@ -480,6 +550,11 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     ids_bad = 3 - np.argsort(-l[:, ::-1], axis=1, kind="stable")[:, :1]
     assert set(ids_bad[0].tolist()) != brute_topk(l[0].tolist(), 1)
     assert set(O.route(l, 1)[0][0].tolist()) == brute_topk(l[0].tolist(), 1)
+
+    # a round-robin map that keeps the linear slots fails the hand-worked rank loads
+    ids = np.repeat(np.arange(8), [10, 0, 3, 5, 2, 7, 1, 4]).astype(np.int32)[:, None]
+    lay = O.dispatch_layout(ids, 8, 4, O.eplb_map(np.zeros(8), 4, 0, "linear"), "round_robin")
+    assert lay["rank_counts"].tolist() != [12, 7, 4, 9]
 
     # dropping the renormalisation (raw softmax probabilities) breaks sum(w) = 1
     l = np.random.default_rng(1).standard_normal((4, 8)).astype(np.float32)
