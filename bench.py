@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--override", action="append", default=[], metavar="FIELD=INT",
                     help="change an integer field of the workload (T, E, R, k, d, I, n_redundant, eplb_placement, "
-                         "expert_placement), e.g. for a small profiling case")
+                         "expert_placement, fp8_dispatch), e.g. for a small profiling case")
     return ap.parse_args()
 
 
@@ -106,6 +106,7 @@ def workload_config(cfg):
             "shared_expert": cfg.shared, "redundant_experts": cfg.n_redundant, "experts_dtype": cfg.dtype,
             "eplb_placement": ("load-aware" if cfg.eplb_placement else "hottest experts") if cfg.n_redundant else None,
             "expert_placement": "round-robin" if cfg.expert_placement == 1 else "linear",
+            "dispatch_dtype": "e4m3" if cfg.dtype == "fp8" or cfg.fp8_dispatch == 1 else cfg.dtype,
             "l2": "flushed between timed steps (512 MiB write)", "parallelism": "independent batch per GPU"}
 
 
@@ -254,7 +255,9 @@ def run_ours(args, world, rank, local):
     dws = torch.empty(dws_b, dtype=torch.uint8, device=dev)
     elt = {moe.MOE_F32: torch.float32, moe.MOE_BF16: torch.bfloat16, moe.MOE_E4M3: torch.uint8}
     xp = torch.empty((N, d), dtype=elt[ex], device=dev)
-    xs = torch.empty((N, d // 128), dtype=torch.float32, device=dev) if ex == moe.MOE_E4M3 else None
+    fp8_dispatch = cfg.fp8_dispatch == 1 and ex == moe.MOE_BF16   # e4m3 send buffer, bf16 rows rebuilt
+    xs = torch.empty((N, d // 128), dtype=torch.float32, device=dev) if ex == moe.MOE_E4M3 or fp8_dispatch else None
+    xq = torch.empty((N, d), dtype=torch.uint8, device=dev) if fp8_dispatch else None
     h = torch.empty((rows, I), dtype=elt[ex] if ex != moe.MOE_BF16 else torch.bfloat16, device=dev)
     hs = torch.empty((rows, I // 128), dtype=torch.float32, device=dev) if ex == moe.MOE_E4M3 else None
     y = torch.empty((rows, d), dtype=torch.float32 if act == moe.MOE_F32 else torch.bfloat16, device=dev)
@@ -269,7 +272,7 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stage_names = ["route", "dispatch_layout", "permute", "expert_gate_up", "expert_down", "combine"]
     launches = {"route": 1, "dispatch_layout": 3 * (2 if cfg.n_redundant else 1) + (1 if mapped else 0),
-                "permute": 1, "expert_gate_up": 1, "expert_down": 1, "combine": 1}
+                "permute": 2 if fp8_dispatch else 1, "expert_gate_up": 1, "expert_down": 1, "combine": 1}
 
     def step(ev):
         ev[0].record(stream)
@@ -285,7 +288,11 @@ def run_ours(args, world, rank, local):
             moe.moe_placement_map(None, E, R, 0, 1, p2l, prank, repc, l2p)
         moe.moe_dispatch_layout(ids, T, k, E, R, eplb, lc, pc, po, rc, ro, r2t, s2r, stats, dws, dws_b, err)
         ev[2].record(stream)
-        moe.moe_permute(x, act, T, d, k, s2r, xp, perm_dt, xs)
+        if fp8_dispatch:
+            moe.moe_permute(x, act, T, d, k, s2r, xq, moe.MOE_E4M3, xs)
+            moe.moe_dequantize_e4m3(xq, xs, N, d, xp)
+        else:
+            moe.moe_permute(x, act, T, d, k, s2r, xp, perm_dt, xs)
         ev[3].record(stream)
         moe.moe_expert_gate_up(xp, xs, po, P, p2l if mapped else None, N, W, x if cfg.shared else None,
                                T_sh, h, hs, err)
@@ -327,7 +334,8 @@ def run_ours(args, world, rank, local):
     # the step itself: moe_layer_forward on inputs resident in HBM (one call, the same
     # kernels without a Python round trip between launches)
     layer = Layer(T, d, E, k, I, R, act, ex, cfg.shared, cfg.n_redundant, pw, keep_aux=False, device=dev,
-                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement)
+                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement,
+                  fp8_dispatch=cfg.fp8_dispatch)
     for _ in range(max(args.warmup, 3)):
         layer.forward(logits, x)
     torch.cuda.synchronize()
@@ -359,6 +367,8 @@ def run_ours(args, world, rank, local):
     dn_flops = 2.0 * rows * I * d
     xb = 4 if act == moe.MOE_F32 else 2
     perm_bytes = T * d * xb + N * d * (1 if cfg.dtype == "fp8" else xb) + (N * d // 128 * 4 if cfg.dtype == "fp8" else 0)
+    if fp8_dispatch:   # e4m3 rows + scales written, read back, bf16 rows written
+        perm_bytes = T * d * xb + 2 * (N * d + N * d // 128 * 4) + N * d * xb
     comb_bytes = N * d * (4 if act == moe.MOE_F32 else 2) + T_sh * d * xb + T * d * xb + N * 8
     route_bytes = T * E * 4 + N * 8
     weight_bound = rows / max(active_logical, 1) < 64   # few rows per expert: weight reads dominate

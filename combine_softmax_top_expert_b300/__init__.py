@@ -17,7 +17,8 @@ __all__ = [
     "LoadStats", "Eplb", "Weights", "Shape", "LayerAux",
     "moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_placement_map",
     "moe_eplb_balanced_map", "moe_eplb_window_update", "moe_dispatch_workspace_size",
-    "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
+    "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
+    "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
     "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
     "moe_selftest_wait_timeout", "EXPORTED",
@@ -35,7 +36,8 @@ _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "
 EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map", "moe_placement_map",
             "moe_eplb_balanced_map",
             "moe_eplb_window_update", "moe_dispatch_workspace_size",
-            "moe_dispatch_layout", "moe_permute", "moe_ffn_workspace_size", "moe_expert_ffn",
+            "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
+    "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
             "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
             "moe_selftest_wait_timeout")
@@ -63,13 +65,13 @@ class Eplb(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     _fields_ = [("dtype", c_i32), ("has_shared", c_i32), ("E_w", c_i64), ("d", c_i64), ("I", c_i64),
-                ("w13", c_vp), ("w2", c_vp), ("s13", c_vp), ("s2", c_vp)]
+                ("w13", c_vp), ("w2", c_vp), ("s13", c_vp), ("s2", c_vp), ("selection_bias", c_vp)]
 
 
 class Shape(ctypes.Structure):
     _fields_ = [("T", c_i64), ("d", c_i64), ("E", c_i64), ("I", c_i64), ("k", c_i32), ("R", c_i32),
                 ("n_redundant", c_i32), ("shared", c_i32), ("act_dtype", c_i32), ("expert_dtype", c_i32),
-                ("eplb_placement", c_i32), ("expert_placement", c_i32)]
+                ("eplb_placement", c_i32), ("expert_placement", c_i32), ("fp8_dispatch", c_i32)]
 
 
 class LayerAux(ctypes.Structure):
@@ -78,7 +80,7 @@ class LayerAux(ctypes.Structure):
                                     "phys_to_logical", "phys_rank", "replica_count", "logical_to_phys")]
 
 
-assert ctypes.sizeof(LoadStats) == 32 and ctypes.sizeof(Weights) == 64 and ctypes.sizeof(Shape) == 64
+assert ctypes.sizeof(LoadStats) == 32 and ctypes.sizeof(Weights) == 72 and ctypes.sizeof(Shape) == 72
 assert ctypes.sizeof(Eplb) == 40
 
 # ------------------------------------------------------------------ loading
@@ -111,6 +113,7 @@ def lib():
             "moe_dispatch_layout_static": (st, [c_vp, c_i64, c_i32, c_i64, c_i32, _P(Eplb)] + [c_vp] * 8
                                            + [c_vp, c_vp]),
             "moe_permute": (st, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp]),
+            "moe_dequantize_e4m3": (st, [c_vp, c_vp, c_i64, c_i64, c_vp, c_vp]),
             "moe_ffn_workspace_size": (sz, [c_i64, c_i64, c_i32]),
             "moe_expert_ffn": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp, c_i64, c_vp,
                                     c_vp, sz, c_vp, c_vp]),
@@ -231,6 +234,10 @@ def moe_dispatch_layout_static(topk_ids, T, k, E, R, eplb, logical_counts, phys_
 def moe_permute(x, x_dt, T, d, k, slot_to_row, x_perm, perm_dt, perm_scales=None, stream=None):
     _check("moe_permute", lib().moe_permute(_p(x), x_dt, T, d, k, _p(slot_to_row), _p(x_perm), perm_dt,
                                             _p(perm_scales), _s(stream)))
+
+
+def moe_dequantize_e4m3(codes, scales, rows, d, out, stream=None):
+    _check("moe_dequantize_e4m3", lib().moe_dequantize_e4m3(_p(codes), _p(scales), rows, d, _p(out), _s(stream)))
 
 
 def moe_ffn_workspace_size(rows, I, dtype) -> int:

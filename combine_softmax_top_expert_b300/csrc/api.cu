@@ -18,6 +18,7 @@ moe_status_t eplb_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int
                       cudaStream_t);
 moe_status_t permute(const void *, moe_dtype_t, int64_t, int64_t, int32_t, const int32_t *, void *, moe_dtype_t,
                      float *, cudaStream_t);
+moe_status_t dequantize_e4m3(const void *, const float *, int64_t, int64_t, void *, cudaStream_t);
 moe_status_t combine(const void *, moe_dtype_t, const int32_t *, const float *, int64_t, int32_t, int64_t,
                      const void *, void *, moe_dtype_t, cudaStream_t);
 
@@ -99,10 +100,10 @@ struct LayerPlan {
   int64_t T, N, P, d, I, E;
   int32_t k, R;
   size_t act_bytes, perm_bytes, y_bytes;
-  bool eplb, shared, balanced, round_robin, mapped;
+  bool eplb, shared, balanced, round_robin, mapped, fp8_dispatch;
   // byte offsets into the workspace
   size_t o_ids, o_w, o_lc, o_pc, o_po, o_rc, o_ro, o_r2t, o_s2r, o_stats, o_p2l, o_prank, o_repc, o_l2p, o_disp,
-      o_xp, o_xs, o_y, o_ffn, total;
+      o_xp, o_xq, o_xs, o_y, o_ffn, total;
 };
 
 static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
@@ -123,6 +124,11 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
   if (s->expert_placement != 0 && s->expert_placement != 1) return false;
   p->round_robin = s->expert_placement == 1;
   p->mapped = p->eplb || p->round_robin;  // physical ids differ from logical ones
+  if (s->fp8_dispatch != 0 && s->fp8_dispatch != 1) return false;
+  // bf16 experts fed from an e4m3 dispatch (e4m3 experts always are)
+  p->fp8_dispatch = s->fp8_dispatch == 1 && s->expert_dtype == MOE_BF16;
+  if (s->fp8_dispatch == 1 && s->expert_dtype == MOE_F32) return false;
+  if (p->fp8_dispatch && s->d % 128) return false;
   p->shared = s->shared != 0;
   p->P = s->E + s->n_redundant;
   p->act_bytes = s->act_dtype == MOE_F32 ? 4 : 2;
@@ -151,7 +157,8 @@ static bool plan_layer(const moe_shape_t *s, LayerPlan *p) {
   p->o_l2p = take((size_t)p->E * 4 * (p->balanced ? 1 + s->n_redundant : 2));
   p->o_disp = take(dispatch_ws_bytes(p->T, p->k, p->P));
   p->o_xp = take((size_t)p->N * p->d * p->perm_bytes);
-  p->o_xs = take(s->expert_dtype == MOE_E4M3 ? (size_t)p->N * (p->d / 128) * 4 : 0);
+  p->o_xq = take(p->fp8_dispatch ? (size_t)p->N * p->d : 0);
+  p->o_xs = take(s->expert_dtype == MOE_E4M3 || p->fp8_dispatch ? (size_t)p->N * (p->d / 128) * 4 : 0);
   p->o_y = take((size_t)rows * p->d * p->y_bytes);
   p->o_ffn = take(ffn_ws_bytes(rows, p->I, s->expert_dtype));
   p->total = o;
@@ -266,7 +273,7 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
   const size_t disp_bytes = dispatch_ws_bytes(p.T, p.k, p.P);
 
   moe_status_t r;
-  if ((r = moe_route(logits, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK) return r;
+  if ((r = moe_route_biased(logits, w->selection_bias, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK) return r;
   moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p, p.balanced ? (int32_t)(1 + p.P - p.E) : 2, p.round_robin ? 1 : 0};
   if (p.eplb) {
     // counts of this batch's logical routing, then the replica map built on them
@@ -284,8 +291,15 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
   if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.mapped ? &map : nullptr, lc, pc, po, rc, ro, r2t, s2r, stats,
                            disp, disp_bytes, err, st)) != MOE_OK)
     return r;
-  const moe_dtype_t perm_dt = s->expert_dtype == MOE_E4M3 ? MOE_E4M3 : s->act_dtype;
-  if ((r = permute(x, s->act_dtype, p.T, p.d, p.k, s2r, xp, perm_dt, xs, st)) != MOE_OK) return r;
+  if (p.fp8_dispatch) {
+    // the send buffer holds e4m3 rows and their scales; the receive side rebuilds bf16 rows
+    void *xq = base + p.o_xq;
+    if ((r = permute(x, s->act_dtype, p.T, p.d, p.k, s2r, xq, MOE_E4M3, xs, st)) != MOE_OK) return r;
+    if ((r = dequantize_e4m3(xq, xs, p.N, p.d, xp, st)) != MOE_OK) return r;
+  } else {
+    const moe_dtype_t perm_dt = s->expert_dtype == MOE_E4M3 ? MOE_E4M3 : s->act_dtype;
+    if ((r = permute(x, s->act_dtype, p.T, p.d, p.k, s2r, xp, perm_dt, xs, st)) != MOE_OK) return r;
+  }
   const int64_t T_sh = p.shared ? p.T : 0;
   if ((r = expert_ffn(xp, xs, po, p.P, p.mapped ? p2l : nullptr, p.N, w, p.shared ? x : nullptr, T_sh, y, fws,
                       ffn_ws_bytes(p.N + T_sh, p.I, s->expert_dtype), err, st)) != MOE_OK)

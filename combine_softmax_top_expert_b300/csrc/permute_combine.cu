@@ -10,6 +10,10 @@
 // batch of 128 tokens spreads over hundreds of blocks; the token's k rows are
 // staged in shared memory and combine keeps eight row loads in flight per thread.
 // Accesses are 16 bytes wide.
+//
+// FP8 dispatch for bf16 experts (section 3.2: tokens travel in FP8, experts and
+// the combine stay in BF16) is the e4m3 permute followed by the receive side,
+// dequant_e4m3_kernel: codes and their group scales back to bf16 rows.
 #include "common.cuh"
 
 namespace moe {
@@ -169,6 +173,41 @@ __global__ void __launch_bounds__(kTok) combine_kernel(const void *__restrict__ 
   }
 }
 
+// OCP e4m3 code -> float, exactly: exponent field e (bias 7) and mantissa m give
+// (1 + m/8) 2^(e-7), or m 2^-9 for e = 0.  (The quantiser saturates, so the NaN
+// codes 0x7F / 0xFF never occur.)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
+  return __uint_as_float(__float_as_uint(v) | ((c & 0x80u) << 24));
+}
+
+// Receive side of the FP8 dispatch: out = bf16_rn(code * scale), the product an
+// IEEE fp32 multiply.  Item i is 8 codes (an 8-byte load, a 16-byte store, so a
+// warp's accesses are contiguous); codes [rows, d] and scales [rows, d/128] are
+// both dense, so item i's scale is scales[i / 16] with no row arithmetic.  Two items
+// per loop trip keep two loads in flight per thread.
+__device__ __forceinline__ uint4 dequant8(uint2 c, float s) {
+  return make_uint4(pack_bf16x2(__fmul_rn(e4m3_to_f32(c.x & 0xFFu), s), __fmul_rn(e4m3_to_f32((c.x >> 8) & 0xFFu), s)),
+                    pack_bf16x2(__fmul_rn(e4m3_to_f32((c.x >> 16) & 0xFFu), s), __fmul_rn(e4m3_to_f32(c.x >> 24), s)),
+                    pack_bf16x2(__fmul_rn(e4m3_to_f32(c.y & 0xFFu), s), __fmul_rn(e4m3_to_f32((c.y >> 8) & 0xFFu), s)),
+                    pack_bf16x2(__fmul_rn(e4m3_to_f32((c.y >> 16) & 0xFFu), s), __fmul_rn(e4m3_to_f32(c.y >> 24), s)));
+}
+
+__global__ void __launch_bounds__(kTok) dequant_e4m3_kernel(const uint2 *__restrict__ q,
+                                                             const float *__restrict__ scales, int64_t items,
+                                                             uint4 *__restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * kTok;
+  int64_t i = (int64_t)blockIdx.x * kTok + threadIdx.x;
+  for (; i + stride < items; i += 2 * stride) {
+    const uint2 c0 = __ldg(q + i), c1 = __ldg(q + i + stride);
+    const float s0 = __ldg(scales + (i >> 4)), s1 = __ldg(scales + ((i + stride) >> 4));
+    out[i] = dequant8(c0, s0);
+    out[i + stride] = dequant8(c1, s1);
+  }
+  if (i < items) out[i] = dequant8(__ldg(q + i), __ldg(scales + (i >> 4)));
+}
+
 // One block per (token, chunk) work item: blocks that finish make room for new
 // ones, so no block waits on another item's stragglers.  (The loops stride only
 // past the grid-size limit.)
@@ -200,6 +239,20 @@ moe_status_t permute(const void *x, moe_dtype_t x_dt, int64_t T, int64_t d, int3
   return MOE_ERR_UNSUPPORTED;
 }
 
+moe_status_t dequantize_e4m3(const void *codes, const float *scales, int64_t rows, int64_t d, void *out,
+                             cudaStream_t st) {
+  if (rows < 0 || d <= 0 || d % 128) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!codes || !scales || !out || !aligned(codes, 16) || !aligned(out, 16) || !aligned(scales, 4))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t items = rows * (d / 8);
+  const int64_t blocks = (items + kTok - 1) / kTok;
+  const int grid = (int)(blocks < 148 * 8 ? blocks : 148 * 8);  // 8 resident blocks per SM, grid-stride past that
+  dequant_e4m3_kernel<<<grid, kTok, 0, st>>>(static_cast<const uint2 *>(codes), scales, items,
+                                             static_cast<uint4 *>(out));
+  return launch_status();
+}
+
 moe_status_t combine(const void *y, moe_dtype_t y_dt, const int32_t *s2r, const float *tw, int64_t T, int32_t k,
                      int64_t d, const void *shared_y, void *out, moe_dtype_t out_dt, cudaStream_t st) {
   if (T < 0 || d <= 0 || d % 8 || k < 1 || k > kMaxK) return MOE_ERR_INVALID_ARG;
@@ -226,6 +279,11 @@ MOE_API moe_status_t moe_permute(const void *x, moe_dtype_t x_dt, int64_t T, int
                                  const int32_t *slot_to_row, void *x_perm, moe_dtype_t perm_dt, float *perm_scales,
                                  moe_stream_t stream) {
   return moe::permute(x, x_dt, T, d, k, slot_to_row, x_perm, perm_dt, perm_scales, moe::as_cuda(stream));
+}
+
+MOE_API moe_status_t moe_dequantize_e4m3(const void *codes, const float *scales, int64_t rows, int64_t d, void *out,
+                                         moe_stream_t stream) {
+  return moe::dequantize_e4m3(codes, scales, rows, d, out, moe::as_cuda(stream));
 }
 
 MOE_API moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_dt, const int32_t *slot_to_row,

@@ -18,8 +18,9 @@ def dtype_code(name: str) -> int:
 class PackedWeights:
     """Packed expert weights (moe_weights_t) for E routed experts (+1 shared)."""
 
-    def __init__(self, E, d, I, dtype: int, shared: bool, device="cuda"):
+    def __init__(self, E, d, I, dtype: int, shared: bool, device="cuda", selection_bias=None):
         self.E, self.d, self.I, self.dtype, self.shared = E, d, I, dtype, shared
+        self.selection_bias = selection_bias   # fp32 [E] on the device, or None
         self.E_w = E + (1 if shared else 0)
         t = _TORCH[dtype]
         self.w13 = torch.empty((self.E_w, 2 * I, d), dtype=t, device=device)
@@ -42,6 +43,7 @@ class PackedWeights:
         w.w13, w.w2 = self.w13.data_ptr(), self.w2.data_ptr()
         w.s13 = self.s13.data_ptr() if self.s13 is not None else None
         w.s2 = self.s2.data_ptr() if self.s2 is not None else None
+        w.selection_bias = self.selection_bias.data_ptr() if self.selection_bias is not None else None
         return w
 
 
@@ -51,11 +53,11 @@ class Layer:
 
     def __init__(self, T, d, E, k, I, R, act_dtype, expert_dtype, shared=False, n_redundant=0,
                  weights: PackedWeights | None = None, keep_aux=True, device="cuda", eplb_placement=0,
-                 expert_placement=0):
+                 expert_placement=0, fp8_dispatch=0):
         s = Shape()
         s.T, s.d, s.E, s.I, s.k, s.R = T, d, E, I, k, R
         s.n_redundant, s.shared, s.act_dtype, s.expert_dtype = n_redundant, int(shared), act_dtype, expert_dtype
-        s.eplb_placement, s.expert_placement = eplb_placement, expert_placement
+        s.eplb_placement, s.expert_placement, s.fp8_dispatch = eplb_placement, expert_placement, fp8_dispatch
         self.shape, self.device = s, device
         self.weights = weights
         self.ws_bytes = moe_layer_workspace_size(s)

@@ -115,6 +115,9 @@ typedef struct {
   const void *w2;
   const float *s13;
   const float *s2;
+  const float *selection_bias; /* [E] fp32 or NULL: moe_layer_forward routes with
+                                  moe_route_biased (experts picked by logit + bias,
+                                  weighted by the unbiased logits); NULL = moe_route */
 } moe_weights_t;
 
 /* Whole-layer shape and precision. */
@@ -136,6 +139,11 @@ typedef struct {
                                statistics; the load-aware map places every expert
                                itself, so with eplb_placement 1 only the statistics
                                change                                                   */
+  int32_t fp8_dispatch;     /* 1 with bf16 experts: tokens are dispatched as e4m3 with
+                               per-128-channel scales (moe_permute to MOE_E4M3) and
+                               turned back into bf16 rows (moe_dequantize_e4m3) for
+                               the experts; needs d % 128 == 0.  e4m3 experts always
+                               take e4m3 rows, so there it changes nothing           */
 } moe_shape_t;
 
 /* Optional device buffers that receive the layer's intermediate results; any
@@ -329,6 +337,15 @@ moe_status_t moe_permute(const void *x, moe_dtype_t x_dt, int64_t T, int64_t d,
                          moe_dtype_t perm_dt, float *perm_scales,
                          moe_stream_t stream);
 
+/* Receive side of an FP8 dispatch to bf16 experts ("6.4 ...", section 3.2: tokens
+ * are dispatched in FP8, the experts and the combine work in BF16).  codes
+ * [rows, d] e4m3 and scales [rows, d/128] fp32, as moe_permute writes them ->
+ * out [rows, d] bf16 with out = bf16(code * scale): the product is an IEEE fp32
+ * multiply, rounded to bf16 to nearest even.  Requires d % 128 == 0, 16-byte
+ * aligned codes and out. */
+moe_status_t moe_dequantize_e4m3(const void *codes, const float *scales, int64_t rows,
+                                 int64_t d, void *out, moe_stream_t stream);
+
 /* Bytes of workspace moe_expert_ffn needs (the intermediate h and tile tables). */
 size_t moe_ffn_workspace_size(int64_t rows, int64_t I, moe_dtype_t expert_dtype);
 
@@ -402,9 +419,10 @@ moe_status_t moe_pack_weights(const void *w_gate, const void *w_up,
 /* Bytes of workspace moe_layer_forward needs. */
 size_t moe_layer_workspace_size(const moe_shape_t *shape);
 
-/* The whole layer forward on one stream: route -> dispatch layout (-> EPLB map
- * on this batch's counts and the physical layout) -> permute -> expert FFN
- * (+ shared expert) -> combine.  logits [T, E] fp32, x [T, d] in act_dtype,
+/* The whole layer forward on one stream: route (with w->selection_bias when set)
+ * -> dispatch layout (-> EPLB map on this batch's counts, or the round-robin
+ * placement, and the physical layout) -> permute (e4m3 + dequantisation with
+ * fp8_dispatch) -> expert FFN (+ shared expert) -> combine.  logits [T, E] fp32, x [T, d] in act_dtype,
  * out [T, d] in act_dtype.  `aux` (nullable, host struct) exposes intermediate
  * results.  ws: moe_layer_workspace_size(shape) bytes, 256-byte aligned.  No host
  * synchronisation happens inside. */

@@ -142,6 +142,7 @@ class LayerConfig:
     n_redundant: int = 0
     eplb_placement: int = 0      # 0: replicas for the hottest experts; 1: load-aware placement
     expert_placement: int = 0    # 0: linear (rank e // (E/R)); 1: round-robin (rank e % R)
+    fp8_dispatch: int = 0        # 1: bf16 workloads dispatch tokens as e4m3 (+ scales)
     dtype: str = "bf16"          # "fp32", "bf16" or "fp8" (e4m3 experts, bf16 in/out)
     zipf_bias: bool = False
     seed: int = 0

@@ -421,6 +421,15 @@ def dequantize_blocks(codes, scales, block: int = 128) -> np.ndarray:
             * scales.astype(np.float64)[:, None, :, None]).reshape(r, c)
 
 
+def dequantize_groups_bf16(codes, scales, group: int = 128) -> np.ndarray:
+    """The receive side of an FP8 dispatch to bf16 experts ("6.4 ...", section 3.2):
+    each code times its group's scale as one IEEE float32 multiply (numpy's float32
+    product), then rounded to bf16 to nearest even.  Returns float64 values."""
+    v = e4m3_decode(codes).astype(np.float32)                 # exact: e4m3 is a subset of float32
+    s = np.repeat(np.asarray(scales, dtype=np.float32), group, axis=1)
+    return round_bf16((v * s).astype(np.float32))
+
+
 def dequantize_groups(codes, scales, group: int = 128) -> np.ndarray:
     v = e4m3_decode(codes)
     rows, n = v.shape
@@ -476,11 +485,13 @@ def _as64(a, kind):
     return a.astype(np.float64)
 
 
-def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
+def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None, selection_bias=None):
     """The layer forward for a workload `cfg` (fields T, d, E, k, I, R, shared,
     n_redundant, dtype, eplb_placement: 1 builds the EPLB map with
-    eplb_balanced_map instead of eplb_map, and expert_placement: 1 places the
-    logical experts round-robin instead of linearly).
+    eplb_balanced_map instead of eplb_map, expert_placement: 1 places the
+    logical experts round-robin instead of linearly, and fp8_dispatch: 1 sends the
+    bf16 workloads' tokens as e4m3 and rebuilds bf16 rows from them).
+    selection_bias [E] (optional) routes with route_selection_bias.
 
     logits: float32 [T, E]; x: [T, d] float32 (fp32) or bf16 bits (uint16);
     weight(which, e) -> logical matrix (which in w_gate, w_up, w_down, ws_gate, ws_up,
@@ -489,7 +500,10 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
     the routing, the layout, the quantised x rows (fp8) and out [len(tokens), d]
     (float64, before the final rounding) plus out_rounded (bf16 values for bf16/fp8)."""
     T, E, k, R = cfg.T, cfg.E, cfg.k, cfg.R
-    ids, w = route(logits, k)
+    if selection_bias is None:
+        ids, w = route(logits, k)
+    else:
+        ids, w = route_selection_bias(logits, selection_bias, k)
     if eplb_enabled is None:
         eplb_enabled = cfg.n_redundant > 0
     placement = "round_robin" if getattr(cfg, "expert_placement", 0) == 1 else "linear"
@@ -512,6 +526,12 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
         xq, xsc = quantize_groups(xs.astype(np.float32))
         res["x_q"], res["x_scales"] = xq, xsc
         xs = dequantize_groups(xq, xsc)
+    x_local = xs          # the shared expert runs where the token lives: never dispatched
+    if mode == "bf16" and getattr(cfg, "fp8_dispatch", 0) == 1:
+        # the routed rows travel in e4m3 (the x rows' quantisation), rebuilt as bf16 rows
+        xq, xsc = quantize_groups(xs.astype(np.float32))
+        res["x_q"], res["x_scales"] = xq, xsc
+        xs = dequantize_groups_bf16(xq, xsc)
 
     def wmat(which, e):
         m = weight(which, e)
@@ -530,7 +550,7 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None):
         y_slots[sel[0], sel[1]] = yv
     out = np.einsum("tj,tjd->td", w[tokens], y_slots)
     if cfg.shared:
-        out = out + swiglu_expert(xs, wmat("ws_gate", 0), wmat("ws_up", 0), wmat("ws_down", 0), mode)
+        out = out + swiglu_expert(x_local, wmat("ws_gate", 0), wmat("ws_up", 0), wmat("ws_down", 0), mode)
     res["out"] = out
     res["out_rounded"] = out if mode == "fp32" else round_bf16(out)
     return res

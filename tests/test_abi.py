@@ -34,8 +34,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.LoadStats) == 32
-    assert ctypes.sizeof(moe.Weights) == 64
-    assert ctypes.sizeof(moe.Shape) == 64
+    assert ctypes.sizeof(moe.Weights) == 72
+    assert ctypes.sizeof(moe.Shape) == 72
     assert ctypes.sizeof(moe.Eplb) == 40
     assert ctypes.sizeof(moe.LayerAux) == 14 * 8
 
@@ -64,6 +64,8 @@ def test_host_validation_without_gpu(lib):
     assert L.moe_placement_map(fake4, 256, 32, 32, 2, fake4, fake4, fake4, fake4, None) == 1  # placement 2
     assert L.moe_placement_map(None, 256, 32, 32, 1, fake4, fake4, fake4, fake4, None) == 1   # hot list, no counts
     assert L.moe_placement_map(None, 256, 30, 0, 1, fake4, fake4, fake4, fake4, None) == 1    # E % R
+    assert L.moe_dequantize_e4m3(fake4, fake4, 4, 200, fake4, None) == 1        # d % 128
+    assert L.moe_dequantize_e4m3(None, None, 0, 128, None, None) == 0           # no rows: nothing queued
     assert L.moe_selftest_wait_timeout(None, 1000000, None, None) == 1          # no error word
     assert L.moe_selftest_wait_timeout(fake4, 10**9, None, None) == 1          # limit above 100 ms
     assert L.moe_permute(None, 1, 0, 128, 2, None, None, 1, None, None) == 0
@@ -112,6 +114,15 @@ def test_empty_batch_and_unsupported_shapes_without_gpu(lib):
     assert moe.moe_layer_workspace_size(s) == 0
     s.expert_placement = 1
     assert moe.moe_layer_workspace_size(s) > 0
+    # FP8 dispatch: bf16 experts take it (workspace grows by the e4m3 rows and scales),
+    # fp32 layers and d % 128 != 0 do not
+    plain = moe.moe_layer_workspace_size(s)
+    s.fp8_dispatch = 1
+    assert moe.moe_layer_workspace_size(s) >= plain + 16 * 2 * 256 + 16 * 2 * 2 * 4
+    s.d = 200
+    assert moe.moe_layer_workspace_size(s) == 0
+    s.d, s.fp8_dispatch = 256, 2
+    assert moe.moe_layer_workspace_size(s) == 0
     # e4m3 experts need d % 256 == 0 (the pair tiles' 256 output features)
     w8 = moe.Weights()
     w8.dtype, w8.has_shared, w8.E_w, w8.d, w8.I = moe.MOE_E4M3, 0, 8, 384, 256

@@ -28,13 +28,15 @@ def device_generated_weights(cfg):
     return weight
 
 
-def run_layer(cfg):
+def run_layer(cfg, bias=None):
     act = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
     ex = dtype_code(cfg.dtype)
-    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
+    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared,
+                       selection_bias=None if bias is None else dev_f32(bias))
     fill_weights(cfg, pw)
     layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw,
-                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement)
+                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement,
+                  fp8_dispatch=cfg.fp8_dispatch)
     logits = mi.make_logits(cfg)
     x = mi.make_x(cfg)
     out = layer.forward(dev_f32(logits), dev_x(cfg, x))
@@ -43,10 +45,10 @@ def run_layer(cfg):
     return layer, logits, x, out.float().cpu().numpy()
 
 
-def check(cfg, sample=None):
-    layer, logits, x, out = run_layer(cfg)
+def check(cfg, sample=None, bias=None):
+    layer, logits, x, out = run_layer(cfg, bias)
     b = {n: t.cpu().numpy() for n, t in layer.bufs.items()}
-    ref = O.layer_forward(cfg, logits, x, device_generated_weights(cfg), tokens=sample)
+    ref = O.layer_forward(cfg, logits, x, device_generated_weights(cfg), tokens=sample, selection_bias=bias)
     lay = ref["layout"]
     assert np.array_equal(b["topk_ids"], ref["topk_ids"])
     assert close(b["topk_w"], ref["topk_w"], F32_TOL)[0] == 0
@@ -127,7 +129,37 @@ def test_layer_bf16_small_balanced_eplb_full():
 def test_layer_bf16_small_round_robin(kw):
     # round-robin base placement: alone (the map only renumbers), with hot-list
     # replicas, and with the load-aware map (only the "before" statistics change)
-    check(mi.config(3).scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=0, expert_placement=1, **kw))
+    base = dict(T=300, d=256, E=16, I=256, R=4, n_redundant=0, expert_placement=1)
+    base.update(kw)
+    check(mi.config(3).scaled(**base))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(shared=True, n_redundant=4)])
+def test_layer_bf16_small_fp8_dispatch(kw):
+    # tokens dispatched as e4m3 with per-128-channel scales, bf16 rows rebuilt for the experts
+    check(mi.config(2).scaled(T=300, d=256, E=16, I=256, R=4, shared=False, fp8_dispatch=1).scaled(**kw))
+
+
+def test_layer_prefill_bf16_skew_fp8_dispatch():
+    check(mi.config(2).scaled(fp8_dispatch=1), sample=sample_tokens(8192, n=3, seed=2))
+
+
+def test_layer_fp8_experts_ignore_fp8_dispatch():
+    cfg = mi.config(4).scaled(T=300, d=256, E=8, I=256, R=4)
+    a = run_layer(cfg)[3]
+    b = run_layer(cfg.scaled(fp8_dispatch=1))[3]
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("ci,kw", [(0, dict()), (2, dict(T=300, d=256, E=16, I=256, R=4))])
+def test_layer_selection_bias(ci, kw):
+    # experts picked by logit + bias, weighted by the unbiased logits; the bias moves
+    # the hottest expert's tokens elsewhere
+    cfg = mi.config(ci).scaled(**kw)
+    bias = np.linspace(-2.0, 1.0, cfg.E).astype(np.float32)
+    layer, ref = check(cfg, bias=bias)
+    plain = O.route(mi.make_logits(cfg), cfg.k)[0]
+    assert not np.array_equal(ref["topk_ids"], plain)
 
 
 def test_layer_decode_bf16():

@@ -232,6 +232,43 @@ def test_layout_round_robin(T, E, R, n_red):
                      "round_robin")
 
 
+# ------------------------------------------------------------------ FP8 dispatch, receive side
+@pytest.mark.parametrize("rows,d", [(1, 128), (37, 384), (4096, 7168), (3, 640)])
+def test_dequantize_e4m3_exact(rows, d):
+    rng = np.random.default_rng(rows + d)
+    codes = rng.integers(0, 256, size=(rows, d)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x7E                          # the quantiser makes no NaN codes
+    if d >= 256:
+        codes[0, :256] = np.where((np.arange(256) & 0x7F) == 0x7F, 0, np.arange(256)).astype(np.uint8)
+    scales = (2.0 ** rng.uniform(-20, 20, size=(rows, d // 128))).astype(np.float32)
+    out = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dequantize_e4m3(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), rows, d, out)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, O.dequantize_groups_bf16(codes, scales))
+
+
+@pytest.mark.parametrize("T,d", [(300, 256), (8192, 7168)])
+def test_fp8_dispatch_round_trip(T, d):
+    """permute to e4m3 then the receive side, against the oracle's quantise + dequantise."""
+    rng = np.random.default_rng(T)
+    k = 4
+    ids, _ = O.route(rng.standard_normal((T, 16)).astype(np.float32), k)
+    lay = O.dispatch_layout(ids, 16, 4)
+    xb = torch.randn((T, d), generator=torch.Generator().manual_seed(T)).bfloat16()
+    N = T * k
+    xq = torch.empty((N, d), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((N, d // 128), dtype=torch.float32, device="cuda")
+    xr = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
+    s2r = torch.from_numpy(lay["slot_to_row"].astype(np.int32)).cuda()
+    moe.moe_permute(xb.cuda(), moe.MOE_BF16, T, d, k, s2r, xq, moe.MOE_E4M3, xs)
+    moe.moe_dequantize_e4m3(xq, xs, N, d, xr)
+    torch.cuda.synchronize()
+    q, sc = O.quantize_groups(xb.float().numpy())
+    want = O.dequantize_groups_bf16(q, sc)[lay["row_to_token"]]
+    assert np.array_equal(xr.float().cpu().numpy().astype(np.float64), want)
+
+
 # ------------------------------------------------------------------ permute / combine
 def layout_for(cfg):
     ids, w = O.route(mi.make_logits(cfg), cfg.k)

@@ -430,6 +430,77 @@ def test_quantize_groups_bound_and_amax():
     assert np.all(np.isin((q.reshape(32, 4, 128) & 0x7F).max(axis=2)[g > 0], [0x7E]))
 
 
+def test_dequantize_groups_bf16_matches_torch():
+    """FP8 dispatch, receive side: torch's e4m3 decode, a float32 multiply and its
+    bf16 conversion give the same values."""
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 256, size=(24, 384)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x7E                          # no NaN codes
+    codes[0, :256] = np.arange(256, dtype=np.uint8)
+    codes[0, :256][(codes[0, :256] & 0x7F) == 0x7F] = 0
+    scales = (2.0 ** rng.uniform(-12, 12, size=(24, 3))).astype(np.float32)
+    got = O.dequantize_groups_bf16(codes, scales)
+    tv = torch.from_numpy(codes).view(torch.float8_e4m3fn).float()
+    ts = torch.from_numpy(np.repeat(scales, 128, axis=1))
+    ref = (tv * ts).bfloat16().double().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_dispatch_lossless_on_the_e4m3_grid():
+    """Tokens whose 128-channel groups hold e4m3 values times 2^-4 with amax 28 have
+    scale 2^-4 exactly, so the e4m3 dispatch returns them unchanged and the layer's
+    output equals the plain bf16 dispatch's."""
+    cfg = mi.config(2).scaled(T=24, d=256, E=4, k=2, I=128, R=2, shared=False, zipf_bias=False)
+    rng = np.random.default_rng(12)
+    grid = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))            # finite non-negative values
+    x = (rng.choice(grid, size=(cfg.T, cfg.d)) * rng.choice([-1.0, 1.0], size=(cfg.T, cfg.d)) / 16.0)
+    x[:, ::128] = 448.0 / 16.0                                       # every group's amax is 28
+    x = x.astype(np.float32)
+    l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
+    wt = tiny_weights(cfg, 13)
+    a = O.layer_forward(cfg, l, x, wt)
+    b = O.layer_forward(cfg.scaled(fp8_dispatch=1), l, x, wt)
+    assert np.all(b["x_scales"] == np.float32(1 / 16))
+    assert np.array_equal(a["out"], b["out"])
+    # off the grid the dispatch rounds: the rows move by at most e4m3's half ulp and
+    # bf16's, and the output changes
+    x2 = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    a2 = O.layer_forward(cfg, l, x2, wt)
+    b2 = O.layer_forward(cfg.scaled(fp8_dispatch=1), l, x2, wt)
+    deq = O.dequantize_groups_bf16(b2["x_q"], b2["x_scales"])
+    sc = np.repeat(b2["x_scales"], 128, axis=1)
+    bound = (np.abs(x2) * 2.0 ** -4 + sc * 2.0 ** -10) * (1 + 2.0 ** -8) + np.abs(x2) * 2.0 ** -8
+    assert np.all(np.abs(deq - x2) <= bound)
+    assert not np.array_equal(a2["out"], b2["out"])
+    # the shared expert is not dispatched: its contribution does not change
+    cs = cfg.scaled(shared=True, E=1, k=1, R=1)
+    l1 = np.zeros((cfg.T, 1), np.float32)
+    a3 = O.layer_forward(cs, l1, x2, wt, eplb_enabled=False)
+    b3 = O.layer_forward(cs.scaled(fp8_dispatch=1), l1, x2, wt, eplb_enabled=False)
+    sh = O.swiglu_expert(x2.astype(np.float64), wt("ws_gate", 0).astype(np.float64),
+                         wt("ws_up", 0).astype(np.float64), wt("ws_down", 0).astype(np.float64), "bf16")
+    w64 = [wt(n, 0).astype(np.float64) for n in ("w_gate", "w_up", "w_down")]
+    deq = O.dequantize_groups_bf16(b3["x_q"], b3["x_scales"])
+    # one expert at weight 1: out = routed FFN of the dispatched rows + shared FFN of x
+    assert np.allclose(a3["out"], O.swiglu_expert(x2.astype(np.float64), *w64, "bf16") + sh, rtol=0, atol=1e-12)
+    assert np.allclose(b3["out"], O.swiglu_expert(deq, *w64, "bf16") + sh, rtol=0, atol=1e-12)
+
+
+def test_layer_selection_bias_special_cases():
+    cfg = mi.config(0)
+    l = mi.make_logits(cfg)
+    x = np.random.default_rng(14).standard_normal((cfg.T, cfg.d)).astype(np.float32)
+    wt = tiny_weights(cfg, 15)
+    plain = O.layer_forward(cfg, l, x, wt)
+    zero = O.layer_forward(cfg, l, x, wt, selection_bias=np.zeros(cfg.E, np.float32))
+    assert np.array_equal(plain["out"], zero["out"])
+    # a bias far below every logit keeps expert 3 out of every selection
+    b = np.zeros(cfg.E, np.float32)
+    b[3] = -1e4
+    res = O.layer_forward(cfg, l, x, wt, selection_bias=b)
+    assert res["layout"]["logical_counts"][3] == 0 and 3 not in res["topk_ids"]
+
+
 def test_quantize_blocks_matches_groups_on_blocks():
     rng = np.random.default_rng(7)
     w = rng.standard_normal((256, 384)).astype(np.float32)
