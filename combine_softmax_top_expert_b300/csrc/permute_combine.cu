@@ -173,39 +173,46 @@ __global__ void __launch_bounds__(kTok) combine_kernel(const void *__restrict__ 
   }
 }
 
-// OCP e4m3 code -> float, exactly: exponent field e (bias 7) and mantissa m give
-// (1 + m/8) 2^(e-7), or m 2^-9 for e = 0.  (The quantiser saturates, so the NaN
-// codes 0x7F / 0xFF never occur.)
-__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
-  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
-  return __uint_as_float(__float_as_uint(v) | ((c & 0x80u) << 24));
+// Two OCP e4m3 codes (bits 0-7 and 8-15) -> f16x2 by the hardware conversion (exact:
+// every e4m3 value is an f16 value), then each times the scale as one IEEE fp32
+// multiply, rounded to bf16 to nearest even.
+__device__ __forceinline__ uint32_t dequant2(uint32_t codes, float s) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes)));
+  const float lo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16)));
+  return pack_bf16x2(__fmul_rn(lo, s), __fmul_rn(hi, s));
 }
 
 // Receive side of the FP8 dispatch: out = bf16_rn(code * scale), the product an
 // IEEE fp32 multiply.  Item i is 8 codes (an 8-byte load, a 16-byte store, so a
 // warp's accesses are contiguous); codes [rows, d] and scales [rows, d/128] are
-// both dense, so item i's scale is scales[i / 16] with no row arithmetic.  Two items
-// per loop trip keep two loads in flight per thread.
+// both dense, so item i's scale is scales[i / 16] with no row arithmetic.  Loads
+// are a third of the traffic here, so each thread keeps four items' loads in
+// flight before it converts and stores them.
 __device__ __forceinline__ uint4 dequant8(uint2 c, float s) {
-  return make_uint4(pack_bf16x2(__fmul_rn(e4m3_to_f32(c.x & 0xFFu), s), __fmul_rn(e4m3_to_f32((c.x >> 8) & 0xFFu), s)),
-                    pack_bf16x2(__fmul_rn(e4m3_to_f32((c.x >> 16) & 0xFFu), s), __fmul_rn(e4m3_to_f32(c.x >> 24), s)),
-                    pack_bf16x2(__fmul_rn(e4m3_to_f32(c.y & 0xFFu), s), __fmul_rn(e4m3_to_f32((c.y >> 8) & 0xFFu), s)),
-                    pack_bf16x2(__fmul_rn(e4m3_to_f32((c.y >> 16) & 0xFFu), s), __fmul_rn(e4m3_to_f32(c.y >> 24), s)));
+  return make_uint4(dequant2(c.x, s), dequant2(c.x >> 16, s), dequant2(c.y, s), dequant2(c.y >> 16, s));
 }
+
+constexpr int kDequantUnroll = 4;
 
 __global__ void __launch_bounds__(kTok) dequant_e4m3_kernel(const uint2 *__restrict__ q,
                                                              const float *__restrict__ scales, int64_t items,
                                                              uint4 *__restrict__ out) {
   const int64_t stride = (int64_t)gridDim.x * kTok;
   int64_t i = (int64_t)blockIdx.x * kTok + threadIdx.x;
-  for (; i + stride < items; i += 2 * stride) {
-    const uint2 c0 = __ldg(q + i), c1 = __ldg(q + i + stride);
-    const float s0 = __ldg(scales + (i >> 4)), s1 = __ldg(scales + ((i + stride) >> 4));
-    out[i] = dequant8(c0, s0);
-    out[i + stride] = dequant8(c1, s1);
+  for (; i + (kDequantUnroll - 1) * stride < items; i += kDequantUnroll * stride) {
+    uint2 c[kDequantUnroll];
+    float s[kDequantUnroll];
+#pragma unroll
+    for (int u = 0; u < kDequantUnroll; ++u) {
+      c[u] = __ldg(q + i + u * stride);
+      s[u] = __ldg(scales + ((i + u * stride) >> 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kDequantUnroll; ++u) out[i + u * stride] = dequant8(c[u], s[u]);
   }
-  if (i < items) out[i] = dequant8(__ldg(q + i), __ldg(scales + (i >> 4)));
+  for (; i < items; i += stride) out[i] = dequant8(__ldg(q + i), __ldg(scales + (i >> 4)));
 }
 
 // One block per (token, chunk) work item: blocks that finish make room for new
