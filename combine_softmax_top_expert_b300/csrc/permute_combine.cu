@@ -6,8 +6,10 @@
 //            (the e4m3 variant quantises the row once per 128-channel group first);
 //   combine  reads the k rows y_perm[slot_to_row[t, j]] (+ the shared expert's row)
 //            and writes out[t] once, accumulating in fp32 in j order.
-// A unit of work is one 256 x 16-byte chunk of one token row, so even a decode
-// batch of 128 tokens spreads over hundreds of blocks; the token's k rows are
+// A unit of work is one chunk of at most 256 16-byte vectors of one token row (the
+// block's threads; the host sizes blocks so a row's chunks are equal, e.g. four
+// 224-vector chunks for d = 7168 rather than three of 256 and a half-empty one),
+// so even a decode batch of 128 tokens spreads over hundreds of blocks; the token's k rows are
 // staged in shared memory and combine keeps eight row loads in flight per thread.
 // Accesses are 16 bytes wide.
 //
@@ -19,7 +21,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTok = 256;      // threads per block = 16-byte vectors per chunk
+constexpr int kTok = 256;      // most threads per block = 16-byte vectors per chunk
 constexpr int kMaxK = 32;
 constexpr int kRowsAhead = 8;  // combine: row loads in flight per thread
 
@@ -38,9 +40,9 @@ __global__ void __launch_bounds__(kTok) permute_copy_kernel(const uint4 *__restr
                                                              int k, const int32_t *__restrict__ slot_to_row,
                                                              uint4 *__restrict__ xp) {
   __shared__ int32_t rows[kMaxK];
-  const int64_t chunks = (vecs + kTok - 1) / kTok;
+  const int64_t chunks = (vecs + blockDim.x - 1) / blockDim.x;
   for (int64_t w = blockIdx.x; w < T * chunks; w += gridDim.x) {
-    const int64_t t = w / chunks, v = (w % chunks) * kTok + threadIdx.x;
+    const int64_t t = w / chunks, v = (w % chunks) * blockDim.x + threadIdx.x;
     stage_rows(slot_to_row, nullptr, t, k, rows, nullptr);
     if (v >= vecs) continue;
     const uint4 val = __ldg(x + t * vecs + v);
@@ -59,9 +61,9 @@ __global__ void __launch_bounds__(kTok) permute_e4m3_kernel(const uint4 *__restr
                                                              uint2 *__restrict__ xq, float *__restrict__ scales) {
   __shared__ int32_t rows[kMaxK];
   const int64_t vecs = d / 8, groups = d / 128;
-  const int64_t chunks = (vecs + kTok - 1) / kTok;
+  const int64_t chunks = (vecs + blockDim.x - 1) / blockDim.x;
   for (int64_t w = blockIdx.x; w < T * chunks; w += gridDim.x) {
-    const int64_t t = w / chunks, v = (w % chunks) * kTok + threadIdx.x;
+    const int64_t t = w / chunks, v = (w % chunks) * blockDim.x + threadIdx.x;
     stage_rows(slot_to_row, nullptr, t, k, rows, nullptr);
     const bool active = v < vecs;
     const uint4 raw = active ? __ldg(x + t * vecs + v) : make_uint4(0u, 0u, 0u, 0u);
@@ -110,9 +112,9 @@ __global__ void __launch_bounds__(kTok) combine_kernel(const void *__restrict__ 
   __shared__ int32_t rows[kMaxK];
   __shared__ float wts[kMaxK];
   const int64_t vecs = d / 8;  // 8 values per vector
-  const int64_t chunks = (vecs + kTok - 1) / kTok;
+  const int64_t chunks = (vecs + blockDim.x - 1) / blockDim.x;
   for (int64_t w = blockIdx.x; w < T * chunks; w += gridDim.x) {
-    const int64_t t = w / chunks, v = (w % chunks) * kTok + threadIdx.x;
+    const int64_t t = w / chunks, v = (w % chunks) * blockDim.x + threadIdx.x;
     stage_rows(s2r, tw, t, k, rows, wts);
     if (v >= vecs) continue;
     float acc[8];
@@ -218,8 +220,18 @@ __global__ void __launch_bounds__(kTok) dequant_e4m3_kernel(const uint2 *__restr
 // One block per (token, chunk) work item: blocks that finish make room for new
 // ones, so no block waits on another item's stragglers.  (The loops stride only
 // past the grid-size limit.)
+// Threads per block for rows of `vecs` 16-byte vectors: split the row into the
+// fewest chunks of at most kTok vectors, each as even as whole warps allow.  A
+// multiple of 32, so 16-lane groups never straddle a chunk.
+inline int chunk_threads(int64_t vecs) {
+  const int64_t chunks = (vecs + kTok - 1) / kTok;
+  const int64_t per = (vecs + chunks - 1) / chunks;
+  return (int)((per + 31) / 32 * 32);
+}
+
 inline int work_grid(int64_t T, int64_t vecs) {
-  const int64_t items = T * ((vecs + kTok - 1) / kTok);
+  const int nt = chunk_threads(vecs);
+  const int64_t items = T * ((vecs + nt - 1) / nt);
   return (int)(items < INT32_MAX ? items : INT32_MAX);
 }
 
@@ -233,13 +245,13 @@ moe_status_t permute(const void *x, moe_dtype_t x_dt, int64_t T, int64_t d, int3
   if (x_dt == perm_dt && (x_dt == MOE_F32 || x_dt == MOE_BF16)) {
     const int64_t bytes = d * (x_dt == MOE_F32 ? 4 : 2);
     if (bytes % 16) return MOE_ERR_INVALID_ARG;
-    permute_copy_kernel<<<work_grid(T, bytes / 16), kTok, 0, st>>>(static_cast<const uint4 *>(x), T, bytes / 16, k,
+    permute_copy_kernel<<<work_grid(T, bytes / 16), chunk_threads(bytes / 16), 0, st>>>(static_cast<const uint4 *>(x), T, bytes / 16, k,
                                                                     slot_to_row, static_cast<uint4 *>(x_perm));
     return launch_status();
   }
   if (x_dt == MOE_BF16 && perm_dt == MOE_E4M3) {
     if (d % 128 || !perm_scales) return MOE_ERR_INVALID_ARG;
-    permute_e4m3_kernel<<<work_grid(T, d / 8), kTok, 0, st>>>(static_cast<const uint4 *>(x), T, d, k, slot_to_row,
+    permute_e4m3_kernel<<<work_grid(T, d / 8), chunk_threads(d / 8), 0, st>>>(static_cast<const uint4 *>(x), T, d, k, slot_to_row,
                                                                static_cast<uint2 *>(x_perm), perm_scales);
     return launch_status();
   }
@@ -266,15 +278,15 @@ moe_status_t combine(const void *y, moe_dtype_t y_dt, const int32_t *s2r, const 
   if (T == 0) return MOE_OK;
   if (!y || !s2r || !tw || !out || !aligned(y, 16) || !aligned(out, 16) || (shared_y && !aligned(shared_y, 16)))
     return MOE_ERR_INVALID_ARG;
-  const int g = work_grid(T, d / 8);
+  const int g = work_grid(T, d / 8), nt = chunk_threads(d / 8);
   if (y_dt == MOE_BF16 && out_dt == MOE_BF16)
-    combine_kernel<true, true><<<g, kTok, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
+    combine_kernel<true, true><<<g, nt, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
   else if (y_dt == MOE_BF16 && out_dt == MOE_F32)
-    combine_kernel<true, false><<<g, kTok, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
+    combine_kernel<true, false><<<g, nt, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
   else if (y_dt == MOE_F32 && out_dt == MOE_F32)
-    combine_kernel<false, false><<<g, kTok, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
+    combine_kernel<false, false><<<g, nt, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
   else if (y_dt == MOE_F32 && out_dt == MOE_BF16)
-    combine_kernel<false, true><<<g, kTok, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
+    combine_kernel<false, true><<<g, nt, 0, st>>>(y, s2r, tw, T, k, d, shared_y, out);
   else
     return MOE_ERR_UNSUPPORTED;
   return launch_status();

@@ -140,6 +140,16 @@ def test_layer_bf16_small_fp8_dispatch(kw):
     check(mi.config(2).scaled(T=300, d=256, E=16, I=256, R=4, shared=False, fp8_dispatch=1).scaled(**kw))
 
 
+@pytest.mark.parametrize("kw", [dict(T=1), dict(T=37, d=128, I=128), dict(T=64, E=4, k=4, R=4, expert_placement=1),
+                                dict(T=50, E=8, R=8, expert_placement=1), dict(T=50, E=8, R=1, expert_placement=1)])
+def test_layer_bf16_edge_cases_new_options(kw):
+    # one token; the smallest d and I; k = E; one expert per rank and one rank under
+    # round-robin placement — with the FP8 dispatch on
+    base = dict(T=300, d=256, E=16, I=256, R=4, shared=False, zipf_bias=False, fp8_dispatch=1)
+    base.update(kw)
+    check(mi.config(2).scaled(**base))
+
+
 def test_layer_prefill_bf16_skew_fp8_dispatch():
     check(mi.config(2).scaled(fp8_dispatch=1), sample=sample_tokens(8192, n=3, seed=2))
 
