@@ -14,6 +14,9 @@ moe_status_t eplb_balanced_map(const int32_t *, int64_t, int32_t, int32_t, int32
                                int32_t *, double *, cudaStream_t);
 moe_status_t placement_map(const int32_t *, int64_t, int32_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *,
                            int32_t *, cudaStream_t);
+moe_status_t route_layout_small(const float *, const float *, int64_t, int64_t, int32_t, int32_t, const moe_eplb_t *,
+                                int32_t *, float *, int32_t *, int32_t *, int32_t *, int32_t *, int32_t *, int32_t *,
+                                int32_t *, moe_load_stats_t *, int32_t *, cudaStream_t);
 moe_status_t eplb_map(const int32_t *, int64_t, int32_t, int32_t, int32_t *, int32_t *, int32_t *, int32_t *,
                       cudaStream_t);
 moe_status_t permute(const void *, moe_dtype_t, int64_t, int64_t, int32_t, const int32_t *, void *, moe_dtype_t,
@@ -273,8 +276,22 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
   const size_t disp_bytes = dispatch_ws_bytes(p.T, p.k, p.P);
 
   moe_status_t r;
-  if ((r = moe_route_biased(logits, w->selection_bias, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK) return r;
   moe_eplb_t map{(int32_t)p.P, p2l, repc, l2p, p.balanced ? (int32_t)(1 + p.P - p.E) : 2, p.round_robin ? 1 : 0};
+  bool laid_out = false;
+  if (!p.eplb) {
+    // no replicas: the map (if any) does not depend on the routing, and a batch of
+    // at most one count chunk is routed and laid out by one launch
+    if (p.round_robin && (r = placement_map(nullptr, p.E, p.R, 0, 1, p2l, prank, repc, l2p, st)) != MOE_OK)
+      return r;
+    r = route_layout_small(logits, w->selection_bias, p.T, p.E, p.k, p.R, p.mapped ? &map : nullptr, ids, tw, lc,
+                           pc, po, rc, ro, r2t, s2r, stats, err, st);
+    if (r == MOE_OK)
+      laid_out = true;
+    else if (r != MOE_ERR_UNSUPPORTED)
+      return r;
+  }
+  if (!laid_out && (r = moe_route_biased(logits, w->selection_bias, p.T, p.E, p.k, ids, tw, err, stream)) != MOE_OK)
+    return r;
   if (p.eplb) {
     // counts of this batch's logical routing, then the replica map built on them
     if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, nullptr, lc, pc, po, rc, ro, r2t, s2r, stats, disp,
@@ -284,12 +301,9 @@ MOE_API moe_status_t moe_layer_forward(const moe_shape_t *s, const float *logits
                    : placement_map(lc, p.E, p.R, (int32_t)(p.P - p.E), p.round_robin ? 1 : 0, p2l, prank, repc,
                                    l2p, st);
     if (r != MOE_OK) return r;
-  } else if (p.round_robin) {
-    // no replicas: the map only renumbers the experts rank-major
-    if ((r = placement_map(nullptr, p.E, p.R, 0, 1, p2l, prank, repc, l2p, st)) != MOE_OK) return r;
   }
-  if ((r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.mapped ? &map : nullptr, lc, pc, po, rc, ro, r2t, s2r, stats,
-                           disp, disp_bytes, err, st)) != MOE_OK)
+  if (!laid_out && (r = dispatch_layout(ids, p.T, p.k, p.E, p.R, p.mapped ? &map : nullptr, lc, pc, po, rc, ro, r2t,
+                                        s2r, stats, disp, disp_bytes, err, st)) != MOE_OK)
     return r;
   if (p.fp8_dispatch) {
     // the send buffer holds e4m3 rows and their scales; the receive side rebuilds bf16 rows

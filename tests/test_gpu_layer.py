@@ -150,6 +150,18 @@ def test_layer_bf16_edge_cases_new_options(kw):
     check(mi.config(2).scaled(**base))
 
 
+@pytest.mark.parametrize("kw", [dict(T=64, E=32, k=8), dict(T=65, E=32, k=8), dict(T=32, E=64, k=8),
+                                dict(T=32, E=96, k=8), dict(T=128, E=32, k=4, R=32, expert_placement=1),
+                                dict(T=64, E=512, k=4, R=8), dict(T=32, E=1024, k=16, R=8)])
+def test_layer_single_launch_route_and_layout_bounds(kw):
+    # small batches (ceil(T/32) * k * ceil(E/32) <= 16, N <= 2048, P <= 512) are
+    # routed and laid out by one launch, others by the separate kernels: both sides
+    # of the bound
+    base = dict(T=300, d=128, E=16, k=8, I=128, R=4, shared=False, zipf_bias=False)
+    base.update(kw)
+    check(mi.config(2).scaled(**base))
+
+
 def test_layer_prefill_bf16_skew_fp8_dispatch():
     check(mi.config(2).scaled(fp8_dispatch=1), sample=sample_tokens(8192, n=3, seed=2))
 
@@ -198,17 +210,25 @@ def test_layer_prefill_fp8_skew():
     ("prefill-shaped bf16 with shared expert and EPLB", dict(T=600, d=512, E=8, k=2, I=256, R=4, shared=True,
                                                             n_redundant=4, zipf_bias=True)),
     ("fp8", dict(T=600, d=512, E=8, k=2, I=256, R=4, dtype="fp8", zipf_bias=True)),
+    ("bf16, load-aware EPLB, round-robin, FP8 dispatch, selection bias",
+     dict(T=300, d=256, E=16, k=4, I=256, R=4, n_redundant=8, eplb_placement=1, expert_placement=1,
+          fp8_dispatch=1, bias=True)),
 ])
 def test_layer_forward_replays_in_a_cuda_graph(name, kw):
     """moe_layer_forward queues work on the caller's stream only (no host syncs, no
     allocation), so a CUDA graph captures it; replays on new inputs copied into the
     captured buffers give exactly what eager calls give."""
+    kw = dict(kw)
+    bias = kw.pop("bias", False)
     cfg = mi.config(2).scaled(**{"shared": False, "zipf_bias": False, "dtype": "bf16", **kw})
     act = moe.MOE_BF16
     ex = dtype_code(cfg.dtype)
-    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared)
+    pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared,
+                       selection_bias=dev_f32(np.linspace(-1, 1, cfg.E)) if bias else None)
     fill_weights(cfg, pw)
-    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw)
+    layer = Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R, act, ex, cfg.shared, cfg.n_redundant, pw,
+                  eplb_placement=cfg.eplb_placement, expert_placement=cfg.expert_placement,
+                  fp8_dispatch=cfg.fp8_dispatch)
     logits_in = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
     x_in = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     batches = []
