@@ -271,7 +271,12 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stage_names = ["route", "dispatch_layout", "permute", "expert_gate_up", "expert_down", "combine"]
-    launches = {"route": 1, "dispatch_layout": 3 * (2 if cfg.n_redundant else 1) + (1 if mapped else 0),
+    # a layout of one count chunk (N <= 2048 slots, <= 512 experts) is one launch, else three
+    def layout_launches(n_exp):
+        return 1 if N <= 2048 and n_exp <= 512 else 3
+
+    launches = {"route": 1, "dispatch_layout": (layout_launches(E) if cfg.n_redundant else 0) + layout_launches(P)
+                + (1 if mapped else 0),
                 "permute": 2 if fp8_dispatch else 1, "expert_gate_up": 1, "expert_down": 1, "combine": 1}
 
     def step(ev):
@@ -335,7 +340,7 @@ def run_ours(args, world, rank, local):
     # small batch without replicas is routed and laid out by a single kernel
     single = (cfg.n_redundant == 0 and N <= 2048 and P <= 512
               and (T + 31) // 32 * k * ((E + 31) // 32) <= 16)
-    layer_launches = sum(launches.values()) - (launches["route"] + 3 - 1 if single else 0)
+    layer_launches = sum(launches.values()) - (1 if single else 0)   # route folded into the layout launch
 
     # the step itself: moe_layer_forward on inputs resident in HBM (one call, the same
     # kernels without a Python round trip between launches)

@@ -281,7 +281,9 @@ __global__ void __launch_bounds__(256) layout_scatter_kernel(const int32_t *__re
 constexpr int kSmallP = 512;
 constexpr int kSmallRouteWork = 16;
 
-template <int VPL>
+// kRoute false: the layout alone, from ids already in global memory (a batch of one
+// count chunk laid out in one launch instead of three).
+template <int VPL, bool kRoute>
 __global__ void __launch_bounds__(1024) route_layout_small_kernel(
     const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int k, int R, int P, PhysMap m,
     const int32_t *p2l, bool base_rr, int32_t *__restrict__ ids, float *__restrict__ w, int32_t *logical_counts,
@@ -295,15 +297,19 @@ __global__ void __launch_bounds__(1024) route_layout_small_kernel(
   __shared__ int32_t rcnt[kSmallP];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t N = (int64_t)T * k;
-  for (int t = warp; t < T; t += 32) {
-    int pick;
-    float wt;
-    rt::route_token<VPL>(logits + (int64_t)t * E, bias, E, k, err, pick, wt);
-    if (lane < k) {
-      ids[t * k + lane] = pick;
-      w[t * k + lane] = wt;
-      sids[t * k + lane] = pick;
+  if (kRoute) {
+    for (int t = warp; t < T; t += 32) {
+      int pick;
+      float wt;
+      rt::route_token<VPL>(logits + (int64_t)t * E, bias, E, k, err, pick, wt);
+      if (lane < k) {
+        ids[t * k + lane] = pick;
+        w[t * k + lane] = wt;
+        sids[t * k + lane] = pick;
+      }
     }
+  } else {
+    for (int s = threadIdx.x; s < N; s += blockDim.x) sids[s] = ids[s];
   }
   for (int i = threadIdx.x; i < kCountWarps * P; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
@@ -525,6 +531,13 @@ moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int6
                                                     align_up((size_t)chunks * P * 4, 256));
   PhysMap m{(int)E, k, eplb ? eplb->replica_count : nullptr, eplb ? eplb->logical_to_phys : nullptr,
             eplb && eplb->max_replicas > 0 ? eplb->max_replicas : 2};
+  if (N > 0 && N <= kChunk && P <= kSmallP) {  // one chunk: count, scan and scatter in one launch
+    route_layout_small_kernel<1, false><<<1, 1024, 0, st>>>(
+        nullptr, nullptr, (int)T, (int)E, k, R, (int)P, m, eplb ? eplb->phys_to_logical : nullptr,
+        eplb != nullptr && eplb->base_placement == 1, const_cast<int32_t *>(topk_ids), nullptr, logical_counts,
+        phys_counts, phys_offsets, rank_counts, rank_offsets, row_to_token, slot_to_row, stats, err);
+    return launch_status();
+  }
   if (chunks > 0) {
     const size_t smem = (size_t)kCountWarps * P * 4;
     if (smem > 48 * 1024) {
@@ -566,7 +579,7 @@ moe_status_t route_layout_small(const float *logits, const float *bias, int64_t 
   const int32_t *p2l = eplb ? eplb->phys_to_logical : nullptr;
   const bool rr = eplb != nullptr && eplb->base_placement == 1;
   rt::with_vpl((int)E, [&](auto vpl) {
-    route_layout_small_kernel<decltype(vpl)::value><<<1, 1024, 0, st>>>(
+    route_layout_small_kernel<decltype(vpl)::value, true><<<1, 1024, 0, st>>>(
         logits, bias, (int)T, (int)E, k, R, (int)P, m, p2l, rr, ids, w, logical_counts, phys_counts, phys_offsets,
         rank_counts, rank_offsets, row_to_token, slot_to_row, stats, err);
   });
