@@ -2,7 +2,8 @@
 //
 // Layout ("6.4 Data parallelism and expert parallelism", section 3.1 step 2 and
 // its figure; section 5.1 busiest card / average): a stable, atomic-free counting
-// sort of the N = T*k slots by physical expert, in three launches.
+// sort of the N = T*k slots by physical expert, in three launches (one, by
+// route_layout_small_kernel below, when the slots fit a single count chunk).
 //
 //   count   one CTA per chunk of 2048 consecutive slots (slot s = t*k + j); each
 //           warp takes 256 slots in batches of 32.  __match_any_sync groups the

@@ -30,13 +30,13 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float(u);
 }
 
+// Warp maximum of 64-bit keys, compared as (high word, low word): the largest high
+// word, then the largest low word among the lanes holding it (two warp reductions).
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    uint64_t w = __shfl_xor_sync(kFull, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
+  const uint32_t hi = static_cast<uint32_t>(v >> 32);
+  const uint32_t mhi = __reduce_max_sync(kFull, hi);
+  const uint32_t mlo = __reduce_max_sync(kFull, hi == mhi ? static_cast<uint32_t>(v) : 0u);
+  return (static_cast<uint64_t>(mhi) << 32) | mlo;
 }
 
 // Route the token whose logits start at `row` (E <= 32 * VPL).  Lane j < k gets the
