@@ -34,6 +34,10 @@ sys.path.insert(0, ROOT)
 import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE layer tokens/s on 1 B300; grouped-GEMM % tensor peak; permute GB/s"
+# The library's path choices that decide how many kernels a layer launches (the
+# layout's count chunk, and the bounds of its one-launch layout and of the routing
+# folded into it); tests/test_multirank.py checks them against csrc/layout.cu.
+LAYOUT_CHUNK_SLOTS, SMALL_LAYOUT_EXPERTS, SMALL_ROUTE_WORK = 2048, 512, 16
 UNIT = "tokens/s"
 
 
@@ -273,7 +277,7 @@ def run_ours(args, world, rank, local):
     stage_names = ["route", "dispatch_layout", "permute", "expert_gate_up", "expert_down", "combine"]
     # a layout of one count chunk (N <= 2048 slots, <= 512 experts) is one launch, else three
     def layout_launches(n_exp):
-        return 1 if N <= 2048 and n_exp <= 512 else 3
+        return 1 if N <= LAYOUT_CHUNK_SLOTS and n_exp <= SMALL_LAYOUT_EXPERTS else 3
 
     launches = {"route": 1, "dispatch_layout": (layout_launches(E) if cfg.n_redundant else 0) + layout_launches(P)
                 + (1 if mapped else 0),
@@ -338,8 +342,8 @@ def run_ours(args, world, rank, local):
 
     # kernels one moe_layer_forward call launches: the per-stage ones, except that a
     # small batch without replicas is routed and laid out by a single kernel
-    single = (cfg.n_redundant == 0 and N <= 2048 and P <= 512
-              and (T + 31) // 32 * k * ((E + 31) // 32) <= 16)
+    single = (cfg.n_redundant == 0 and N <= LAYOUT_CHUNK_SLOTS and P <= SMALL_LAYOUT_EXPERTS
+              and (T + 31) // 32 * k * ((E + 31) // 32) <= SMALL_ROUTE_WORK)
     layer_launches = sum(launches.values()) - (1 if single else 0)   # route folded into the layout launch
 
     # the step itself: moe_layer_forward on inputs resident in HBM (one call, the same

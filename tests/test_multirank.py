@@ -1,6 +1,7 @@
 """The multi-rank path of bench.py on CPU: two gloo ranks, one process each, with
 the environment torchrun gives them (RANK, WORLD_SIZE, LOCAL_RANK, MASTER_*), as
-the benchmark runs with one GPU per rank.  No GPU is used."""
+the benchmark runs with one GPU per rank; and the benchmark's host-side
+bookkeeping.  No GPU is used."""
 import json
 import multiprocessing as mp
 import os
@@ -54,6 +55,22 @@ def test_weak_scaling_throughput():
     # 2 ranks x 128 tokens x 10 steps in 20 ms (the slowest rank) = 128,000 tokens/s
     assert bench.job_throughput(2, 128, 10, 20.0) == pytest.approx(128000.0)
     assert bench.job_throughput(1, 128, 10, 20.0) == pytest.approx(64000.0)
+
+
+def test_launch_count_thresholds_match_the_library():
+    """bench.py counts a layer's kernels from the library's path choices: its copies
+    of the thresholds must be the ones the CUDA source uses."""
+    import re
+    sys.path.insert(0, ROOT)
+    import bench
+    src = open(os.path.join(ROOT, "combine_softmax_top_expert_b300", "csrc", "layout.cu")).read()
+
+    def const(name):
+        return int(re.search(r"constexpr int " + name + r" = (\d+);", src).group(1))
+
+    assert const("kChunk") == bench.LAYOUT_CHUNK_SLOTS
+    assert const("kSmallP") == bench.SMALL_LAYOUT_EXPERTS
+    assert const("kSmallRouteWork") == bench.SMALL_ROUTE_WORK
 
 
 def test_reference_arm_under_torchrun_prints_once():
