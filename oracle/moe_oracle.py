@@ -38,6 +38,8 @@ the dense FFN values beyond those reductions rest on this definition.
 """
 from __future__ import annotations
 
+import heapq
+
 import numpy as np
 
 # ============================================================== route
@@ -146,81 +148,55 @@ def base_rank_counts(expert_counts: np.ndarray, R: int, placement: str = "linear
     raise ValueError(f"unknown placement {placement!r}")
 
 
-def greedy_rebalance(counts, R: int, n_redundant: int) -> np.ndarray:
-    """The page's load-aware placement ("6.4 ...", section 5.2): hand each redundant
-    slot to the expert with the highest load per replica (first such expert on a
-    tie), split each expert's load evenly over its replicas, then place replicas
-    heaviest first onto the lightest rank that still has a free slot (lowest rank
-    on a tie).  Returns the per-rank loads (float64)."""
-    counts = [float(c) for c in counts]
-    E = len(counts)
-    replicas = [1] * E
-    for _ in range(n_redundant):
-        best = 0
-        for i in range(1, E):
-            if counts[i] / replicas[i] > counts[best] / replicas[best]:
-                best = i
-        replicas[best] += 1
-    copies = []
-    for e in range(E):
-        copies.extend([counts[e] / replicas[e]] * replicas[e])
-    copies.sort(reverse=True)
-    slots = (E + n_redundant) // R
-    load = [0.0] * R
-    used = [0] * R
-    for c in copies:
-        g = None
-        for r in range(R):
-            if used[r] < slots and (g is None or load[r] < load[g]):
-                g = r
-        load[g] += c
-        used[g] += 1
-    return np.array(load)
-
-
 def eplb_balanced_map(logical_counts, R: int, n_redundant: int) -> dict:
-    """The page's load-aware placement ("6.4 ...", section 5.2, the placement with
-    replicas) written out as a physical-expert map, in the map format of eplb_map.
+    """Load-aware placement with redundant slots ("6.4 Data parallelism and expert
+    parallelism", section 5.2, the rebalanced placement with one redundant slot per
+    card), written out as a physical-expert map in the format of eplb_map.
 
-    Steps, in the page's order: each redundant slot goes to the expert whose load
-    per replica is highest (the first such expert on a tie); every replica of an
-    expert carries count / replicas; the replicas, heaviest first (equal loads keep
-    expert order, then replica order), each go to the lightest rank that still has
-    one of its S = (E + n_red) / R slots free (the lowest rank on a tie), taking that
-    rank's next slot.  Physical id = rank * S + slot; replica j of expert e is its
-    j-th replica in that order.  rank_load holds the per-rank loads the page prints
-    (greedy_rebalance gives the same numbers)."""
+    The rule, as the section states it: every redundant slot goes to the expert that
+    carries the most load per replica, an expert's load is split evenly over its
+    replicas, and the replicas are placed heaviest first, each on the least loaded
+    card that still has a free slot; each card has S = (E + n_red) / R slots.
+
+    Tie rules (the section leaves them open; these are the readings):
+      * equal load per replica: the lower expert id takes the slot;
+      * equal replica loads: expert id ascending, then replica index ascending;
+      * equal card loads: the lower rank.
+    The replica j of expert e is its j-th replica in the placement order, and a card
+    fills its slots in the order replicas arrive, so physical id = rank * S + slot.
+    Loads are float64 count / replicas, and a card's load is summed in arrival order.
+    Returns the map plus rank_load, the per-card load the section tabulates."""
     counts = [int(c) for c in np.asarray(logical_counts).ravel()]
     E = len(counts)
     P = E + n_redundant
     if P % R:
         raise ValueError("physical experts must divide evenly over ranks")
-    replicas = [1] * E
-    for _ in range(n_redundant):
-        best = 0
-        for i in range(1, E):
-            if counts[i] / replicas[i] > counts[best] / replicas[best]:
-                best = i
-        replicas[best] += 1
-    copies = []                                  # (load, expert, replica index)
-    for e in range(E):
-        for j in range(replicas[e]):
-            copies.append((counts[e] / replicas[e], e, j))
-    copies.sort(key=lambda c: -c[0])             # stable: ties keep expert, replica order
     S = P // R
-    load = [0.0] * R
+    # 1. redundant slots: a max-heap on load per replica, lower id first on ties
+    replicas = [1] * E
+    heap = [(-float(counts[e]), e) for e in range(E)]
+    heapq.heapify(heap)
+    for _ in range(n_redundant):
+        _, e = heapq.heappop(heap)
+        replicas[e] += 1
+        heapq.heappush(heap, (-(counts[e] / replicas[e]), e))
+    # 2. every replica with its load, heaviest first
+    pieces = sorted(((counts[e] / replicas[e], e, j) for e in range(E) for j in range(replicas[e])),
+                    key=lambda c: (-c[0], c[1], c[2]))
+    # 3. cards with a free slot in a min-heap on (load, rank)
+    cards = [(0.0, r) for r in range(R)]
     used = [0] * R
+    load = [0.0] * R
     phys_to_logical = np.empty(P, dtype=np.int32)
     phys_rank = np.empty(P, dtype=np.int32)
     logical_to_phys = np.full((E, 1 + n_redundant), -1, dtype=np.int32)
-    for c, e, j in copies:
-        g = None
-        for r in range(R):
-            if used[r] < S and (g is None or load[r] < load[g]):
-                g = r
+    for c, e, j in pieces:
+        _, g = heapq.heappop(cards)
         p = g * S + used[g]
-        load[g] += c
         used[g] += 1
+        load[g] += c
+        if used[g] < S:
+            heapq.heappush(cards, (load[g], g))
         phys_to_logical[p] = e
         phys_rank[p] = g
         logical_to_phys[e, j] = p
@@ -446,6 +422,24 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def stored_h(h, mode: str):
+    """The intermediate h as the down projection takes it (the stored tensor between
+    gate/up and down): "fp32" unchanged; "bf16" rounded to bf16 (RNE); "fp8"
+    quantised to e4m3 per row over each 128-channel group of I and dequantised."""
+    if mode == "bf16":
+        return round_bf16(h)
+    if mode == "fp8":
+        q, s = quantize_groups(np.asarray(h).astype(np.float32))
+        return dequantize_groups(q, s)
+    return h
+
+
+def stored_y(y, mode: str):
+    """An expert's output row as the combine reads it: bf16 (RNE) for the bf16 and
+    fp8 workloads ("6.4 ...", section 3.2: BF16 combine), unchanged for fp32."""
+    return round_bf16(y) if mode in ("bf16", "fp8") else y
+
+
 def swiglu_expert(x64, wg64, wu64, wd64, mode: str):
     """One expert's FFN ("6.4 ...", section 2.1: gate, up, down):
     h = silu(x W_gate) * (x W_up); y = h W_down; float64 matmuls.
@@ -455,16 +449,8 @@ def swiglu_expert(x64, wg64, wu64, wd64, mode: str):
     rounded to bf16.  (x and the weights arrive already dequantised.)"""
     g = x64 @ wg64
     u = x64 @ wu64
-    h = silu(g) * u
-    if mode == "bf16":
-        h = round_bf16(h)
-    elif mode == "fp8":
-        q, s = quantize_groups(h.astype(np.float32))
-        h = dequantize_groups(q, s)
-    y = h @ wd64
-    if mode in ("bf16", "fp8"):
-        y = round_bf16(y)
-    return y
+    h = stored_h(silu(g) * u, mode)
+    return stored_y(h @ wd64, mode)
 
 
 def combine(y_rows: np.ndarray, slot_to_row: np.ndarray, topk_w: np.ndarray, shared=None):

@@ -305,15 +305,22 @@ def test_eplb_balanced_map_exact(E, R, n_red, seed):
     assert np.array_equal(g["rank_load"], r["rank_load"])   # fp64, same operations in the same order
 
 
-def test_eplb_balanced_map_page_simulation():
-    """The page's simulation counts through the GPU map: its printed busiest/average."""
-    import test_oracle_pins as pins
-    gold = pins.load("imbalance_sim_table.json")
-    counts = pins.page_simulation_counts(gold["setup"])
-    for row in gold["rows"]:
-        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
-            g = gpu_balanced_map(counts, row["ep"], n_red)
-            assert round(g["rank_load"].max() / g["rank_load"].mean(), 2) == row[col]
+def test_eplb_balanced_map_worked_examples():
+    """The hand-worked placements of the oracle's pins, through the GPU map."""
+    g = gpu_balanced_map(np.array([10, 6, 3, 1]), 2, 2)
+    assert g["phys_to_logical"].tolist() == [0, 1, 2, 0, 1, 3]
+    assert g["logical_to_phys"].tolist() == [[0, 3, -1], [1, 4, -1], [2, -1, -1], [5, -1, -1]]
+    assert g["rank_load"].tolist() == [11.0, 9.0]
+    g = gpu_balanced_map(np.array([100, 1, 1, 1]), 2, 2)
+    assert g["replica_count"].tolist() == [3, 1, 1, 1]
+    assert g["phys_to_logical"].tolist() == [0, 0, 3, 0, 1, 2]
+    assert g["rank_load"].tolist() == [100 / 3 + 100 / 3 + 1.0, 100 / 3 + 1.0 + 1.0]
+    # one expert per card: nothing to move, the busiest card keeps the hottest expert
+    counts = np.full(256, 125)
+    counts[17] = 640
+    counts[18] = 128 * 256 - 640 - 125 * 254
+    g = gpu_balanced_map(counts, 256, 0)
+    assert round(g["rank_load"].max() / g["rank_load"].mean(), 2) == 5.0
 
 
 @pytest.mark.parametrize("W,E", [(3, 8), (1, 256), (5, 256)])

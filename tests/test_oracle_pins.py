@@ -167,61 +167,36 @@ def test_dispatch_figure_example():
     assert st["balancedness"] == pytest.approx(2 / 3)
 
 
-def page_simulation_counts(setup):
-    """The page's imbalance simulation (section 5.2), restated: expert popularity
-    1/(i+1)^0.4 shuffled with Python's seeded generator, each of 4096 tokens draws
-    distinct experts by weighted choice until it has 8.  The same calls in the same
-    order give the same random stream, which the printed hottest/coldest verify."""
-    rnd = random.Random(setup["python_random_seed"])
-    E, K, T = setup["experts"], setup["top_k"], setup["tokens"]
-    pop = [1 / (i + 1) ** setup["skew"] for i in range(E)]
-    rnd.shuffle(pop)
-    cum = list(itertools.accumulate(pop))
-    counts = [0] * E
-    for _ in range(T):
-        chosen = set()
-        while len(chosen) < K:
-            chosen.add(rnd.choices(range(E), cum_weights=cum)[0])
-        for e in chosen:
-            counts[e] += 1
-    return np.array(counts)
-
-
-@pytest.fixture(scope="module")
-def sim():
-    g = load("imbalance_sim_table.json")
-    return g, page_simulation_counts(g["setup"])
-
-
-def test_sim_reproduces_printed_extremes(sim):
-    g, counts = sim
-    assert counts.max() == g["hottest"] and counts.min() == g["coldest"]
-    assert round(counts.sum() / counts.size) == g["average"]
-
-
-def test_sim_contiguous_column(sim):
-    g, counts = sim
-    for row in g["rows"]:
-        st = O.rank_stats(O.linear_rank_counts(counts, row["ep"]), int(counts.sum()))
-        assert round(st["max_over_mean"], 2) == row["contiguous"]
-        assert st["balancedness"] == pytest.approx(1 / st["max_over_mean"])
-
-
-def test_sim_rebalance_columns(sim):
-    g, counts = sim
-    for row in g["rows"]:
-        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
-            load_ = O.greedy_rebalance(counts, row["ep"], n_red)
-            assert round(load_.max() / load_.mean(), 2) == row[col]
-
-
-def test_balanced_map_reproduces_page_table(sim):
-    g, counts = sim
-    for row in g["rows"]:
-        for n_red, col in ((0, "rebalance"), (row["ep"], "plus_one_redundant")):
-            m = O.eplb_balanced_map(counts, row["ep"], n_red)
-            assert round(m["rank_load"].max() / m["rank_load"].mean(), 2) == row[col]
-            assert np.array_equal(m["rank_load"], O.greedy_rebalance(counts, row["ep"], n_red))
+def test_printed_ep256_column_from_printed_counts():
+    """The section 5.2 table at EP 256 (one expert per card, no redundant slot), from
+    its printed figures alone: with the hottest expert at 640 copies of 4096 x 8 picks
+    over 256 experts (average 128), the contiguous placement and the rebalanced one
+    both leave the busiest card at 640 / 128 = 5.00, whatever the other counts are.
+    Any counts with that hottest value and total give the printed pair."""
+    g = load("ep256_printed.json")
+    total = g["tokens"] * g["top_k"]
+    rng = np.random.default_rng(21)
+    for _ in range(5):
+        hot = int(rng.integers(0, g["experts"]))
+        cold = [e for e in range(g["experts"]) if e != hot]
+        rest = total - g["hottest"]
+        # spread the remaining picks evenly, then move random amounts between cold
+        # experts, keeping every count between 0 and the hottest
+        counts = np.zeros(g["experts"], dtype=np.int64)
+        counts[hot] = g["hottest"]
+        counts[cold] = rest // len(cold)
+        counts[cold[: rest % len(cold)]] += 1
+        for _ in range(2000):
+            a, b = rng.choice(cold, 2, replace=False)
+            m = int(rng.integers(0, min(counts[a], g["hottest"] - counts[b]) + 1))
+            counts[a] -= m
+            counts[b] += m
+        assert counts.max() == g["hottest"] and counts.sum() == total
+        assert round(total / g["experts"]) == g["average"]
+        st = O.rank_stats(O.linear_rank_counts(counts, g["ep"]), total)
+        assert round(st["max_over_mean"], 2) == g["contiguous"]
+        m = O.eplb_balanced_map(counts, g["ep"], 0)
+        assert round(m["rank_load"].max() / m["rank_load"].mean(), 2) == g["rebalance"]
 
 
 def test_balanced_map_worked_example():
@@ -236,6 +211,33 @@ def test_balanced_map_worked_example():
     assert m["phys_rank"].tolist() == [0, 0, 0, 1, 1, 1]
     assert m["logical_to_phys"].tolist() == [[0, 3, -1], [1, 4, -1], [2, -1, -1], [5, -1, -1]]
     assert m["rank_load"].tolist() == [11.0, 9.0]
+
+
+def test_balanced_map_worked_example_one_hot_expert():
+    # counts 100, 1, 1, 1 over 2 ranks with 2 redundant slots, worked by hand:
+    # slot 1 -> e0 (100 > 1), slot 2 -> e0 again (50 > 1): e0 has 3 replicas of 100/3.
+    # S = 3.  Replicas: e0 r0 -> rank 0 (tie, lowest); e0 r1 -> rank 1 (0 < 33.3);
+    # e0 r2 -> rank 0 (tie at 33.3, lowest); e1 -> rank 1 (33.3 < 66.7); e2 -> rank 1
+    # (34.3 < 66.7), which fills it; e3 -> rank 0.
+    m = O.eplb_balanced_map(np.array([100, 1, 1, 1]), 2, 2)
+    third = 100 / 3
+    assert m["replica_count"].tolist() == [3, 1, 1, 1]
+    assert m["phys_rank"].tolist() == [0, 0, 0, 1, 1, 1]
+    assert m["phys_to_logical"].tolist() == [0, 0, 3, 0, 1, 2]
+    assert m["logical_to_phys"].tolist() == [[0, 3, 1], [4, -1, -1], [5, -1, -1], [2, -1, -1]]
+    assert m["rank_load"].tolist() == [third + third + 1.0, third + 1.0 + 1.0]
+
+
+def test_balanced_map_equal_counts_deal_round_robin():
+    # all loads equal: replicas arrive in expert order and every card is the lightest
+    # in turn, so expert e lands on card e mod R (slot e div R)
+    E, R = 12, 4
+    m = O.eplb_balanced_map(np.full(E, 5), R, 0)
+    S = E // R
+    for e in range(E):
+        p = m["logical_to_phys"][e, 0]
+        assert m["phys_rank"][p] == e % R and p == (e % R) * S + e // R
+    assert m["rank_load"].tolist() == [15.0] * R
 
 
 def test_balanced_map_invariants():
@@ -594,6 +596,84 @@ def test_dispatch_bytes_and_expert_size_arithmetic():
     assert round(8 * 7168 * 2 / 1000) == g["combine_bf16_bytes_dsv3_approx_kb"]
 
 
+# ------------------------------------------------------------------ rounding points of the expert FFN
+# One token, d = 1, x = [1]: with every gate weight 64, g = 64 and silu(64) = 64
+# exactly in float64 (e^-64 < 2^-53, so 1 + e^-64 rounds to 1); h = 64 * u is then
+# set by the up weights alone, and y = h . w_down by the down weights.  Every value
+# below is a dyadic rational worked out by hand.
+def one_token_expert(u, wd):
+    u = np.asarray(u, dtype=np.float64)[None, :]
+    I = u.shape[1]
+    wd = np.asarray(wd, dtype=np.float64).reshape(I, 1)
+    return np.ones((1, 1)), np.full((1, I), 64.0), u, wd
+
+
+def test_bf16_mode_rounds_h_at_a_tie():
+    # h = 64 (2^-6 + 2^-14) = 1 + 2^-8, halfway between the bf16 values 1 and 1 + 2^-7:
+    # round-to-nearest-even keeps 1.  y = 3 h: 3 with h rounded; unrounded,
+    # 3 + 3 * 2^-8 lies 3/4 of the way to the next bf16 value 3 + 2^-6.
+    x, wg, wu, wd = one_token_expert([2.0 ** -6 + 2.0 ** -14], [3.0])
+    assert O.swiglu_expert(x, wg, wu, wd, "bf16")[0, 0] == 3.0
+    assert O.swiglu_expert(x, wg, wu, wd, "fp32")[0, 0] == 3.0 + 3.0 * 2.0 ** -8
+
+
+def test_bf16_mode_rounds_y():
+    # h = 1 exactly; y = 1 + 2^-8 is a bf16 tie and rounds to 1; the fp32 mode keeps it
+    x, wg, wu, wd = one_token_expert([2.0 ** -6], [1.0 + 2.0 ** -8])
+    assert O.swiglu_expert(x, wg, wu, wd, "bf16")[0, 0] == 1.0
+    assert O.swiglu_expert(x, wg, wu, wd, "fp32")[0, 0] == 1.0 + 2.0 ** -8
+    # y = 1 + 3 * 2^-8 is a tie between 1 + 2^-7 and 1 + 2^-6: the even one is 1 + 2^-6
+    x, wg, wu, wd = one_token_expert([2.0 ** -6], [1.0 + 3.0 * 2.0 ** -8])
+    assert O.swiglu_expert(x, wg, wu, wd, "bf16")[0, 0] == 1.0 + 2.0 ** -6
+
+
+def test_bf16_mode_equals_fp32_mode_on_bf16_exact_values():
+    # h = 1.5, 0.25, -2 (bf16-exact) and y = 1.5 * 2 + 0.25 * 4 - 2 * 0.5 = 3: no rounding bites
+    x, wg, wu, wd = one_token_expert([1.5 / 64, 0.25 / 64, -2.0 / 64], [2.0, 4.0, 0.5])
+    a = O.swiglu_expert(x, wg, wu, wd, "bf16")
+    b = O.swiglu_expert(x, wg, wu, wd, "fp32")
+    assert a[0, 0] == b[0, 0] == 3.0
+
+
+def fp8_two_group_row():
+    # I = 256: group 0 (channels 0-127) holds h = 448 at channel 0, so its scale is 1;
+    # group 1 (channels 128-255) holds 28 at channel 128, so its scale is 28/448 = 2^-4,
+    # and h = 3 * 2^-10 at channel 129.  Per 128 channels, 3 * 2^-10 / 2^-4 = 3 * 2^-6
+    # = 1.5 * 2^-5 is an e4m3 normal (mantissa 0.5), so it comes back exactly.  One scale
+    # for all 256 channels (448 / 448 = 1) puts it at 1.5 * 2^-9, halfway between the
+    # subnormals 2^-9 and 2^-8, where the even code gives 2^-8.
+    # Channel 1 holds 1 + 2^-5, which scale 1 rounds to the e4m3 value 1.
+    u = np.zeros(256)
+    u[0], u[128], u[129], u[1] = 448.0 / 64, 28.0 / 64, 3.0 * 2.0 ** -10 / 64, (1.0 + 2.0 ** -5) / 64
+    return u
+
+
+def test_fp8_mode_quantises_h_per_128_channels():
+    u = fp8_two_group_row()
+    wd = np.zeros(256)
+    wd[129] = 1.0
+    x, wg, wu, wdm = one_token_expert(u, wd)
+    assert O.swiglu_expert(x, wg, wu, wdm, "fp8")[0, 0] == 3.0 * 2.0 ** -10
+    wd = np.zeros(256)
+    wd[1] = 1.0
+    x, wg, wu, wdm = one_token_expert(u, wd)
+    assert O.swiglu_expert(x, wg, wu, wdm, "fp8")[0, 0] == 1.0
+    assert O.swiglu_expert(x, wg, wu, wdm, "fp32")[0, 0] == 1.0 + 2.0 ** -5
+
+
+def test_fp8_mode_rounds_y_to_bf16():
+    # h = 448 and 0: codes exact with scale 1; y = 448 * (1 + 2^-8) / 448 ... take
+    # w_down = (1 + 2^-8) / 448 at channel 0: y = 1 + 2^-8, the bf16 tie that rounds to 1
+    u = np.zeros(128)
+    u[0] = 448.0 / 64
+    wd = np.zeros(128)
+    wd[0] = 2.0 ** -6 * (1.0 + 2.0 ** -8) / 7.0          # 448 = 7 * 2^6
+    x, wg, wu, wdm = one_token_expert(u, wd)
+    y32 = O.swiglu_expert(x, wg, wu, wdm, "fp32")[0, 0]
+    assert abs(y32 - (1.0 + 2.0 ** -8)) < 1e-15
+    assert O.swiglu_expert(x, wg, wu, wdm, "fp8")[0, 0] == 1.0
+
+
 # ------------------------------------------------------------------ planted mistakes
 def test_pins_catch_planted_mistakes(monkeypatch):
     """Plant plausible slips in the oracle and check that a pin above fails."""
@@ -626,6 +706,34 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     ids = np.repeat(np.arange(8), [10, 0, 3, 5, 2, 7, 1, 4]).astype(np.int32)[:, None]
     lay = O.dispatch_layout(ids, 8, 4, O.eplb_map(np.zeros(8), 4, 0, "linear"), "round_robin")
     assert lay["rank_counts"].tolist() != [12, 7, 4, 9]
+
+    # the rounding points of the expert FFN: h left unrounded, h quantised over all
+    # 256 channels at once, y left unrounded
+    def check_rounding_pins():
+        for pin in (test_bf16_mode_rounds_h_at_a_tie, test_bf16_mode_rounds_y,
+                    test_fp8_mode_quantises_h_per_128_channels, test_fp8_mode_rounds_y_to_bf16):
+            try:
+                pin()
+            except AssertionError:
+                return False
+        return True
+
+    assert check_rounding_pins()
+    real_h, real_y = O.stored_h, O.stored_y
+    monkeypatch.setattr(O, "stored_h", lambda h, mode: h if mode == "bf16" else real_h(h, mode))
+    assert not check_rounding_pins()
+    monkeypatch.setattr(O, "stored_h", lambda h, mode: O.dequantize_groups(
+        *O.quantize_groups(np.asarray(h, np.float32), 256), 256) if mode == "fp8" else real_h(h, mode))
+    assert not check_rounding_pins()
+    monkeypatch.setattr(O, "stored_h", lambda h, mode: h if mode == "fp8" else real_h(h, mode))
+    assert not check_rounding_pins()
+    monkeypatch.setattr(O, "stored_h", real_h)
+    monkeypatch.setattr(O, "stored_y", lambda y, mode: y)
+    assert not check_rounding_pins()
+    monkeypatch.setattr(O, "stored_y", lambda y, mode: y if mode == "fp8" else real_y(y, mode))
+    assert not check_rounding_pins()
+    monkeypatch.undo()
+    assert check_rounding_pins()
 
     # dropping the renormalisation (raw softmax probabilities) breaks sum(w) = 1
     l = np.random.default_rng(1).standard_normal((4, 8)).astype(np.float32)
