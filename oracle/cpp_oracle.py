@@ -1,0 +1,408 @@
+"""The C++ float64 oracle (oracle/moe_oracle.cpp) behind the same Python API as the
+numpy oracle (oracle/moe_oracle.py), so that one set of pins runs against both.
+
+Test infrastructure only: the tests, the package's smoke check and the benchmark's
+CPU legs use it.  This module marshals arrays into the C ABI and builds the result
+dicts; every step of the arithmetic runs in the C++ library.  The library is built
+on first use (g++) when it is missing or older than its source.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_vp = C.c_void_p
+_i32, _i64 = C.c_int32, C.c_int64
+
+WEIGHT_FN = C.CFUNCTYPE(C.c_void_p, C.c_int32, C.c_int32, C.POINTER(C.c_int32))
+_WHICH = ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
+_MODE = {"fp32": 0, "bf16": 1, "fp8": 2}
+
+
+class LayerCfg(C.Structure):
+    _fields_ = [("T", _i64), ("d", _i64), ("E", _i64), ("I", _i64), ("k", _i32), ("R", _i32), ("shared", _i32),
+                ("n_red", _i32), ("mode", _i32), ("eplb", _i32), ("eplb_placement", _i32),
+                ("expert_placement", _i32), ("fp8_dispatch", _i32), ("threads", _i32)]
+
+
+class LayerOut(C.Structure):
+    _fields_ = [("topk_ids", _vp), ("topk_w", _vp), ("logical_counts", _vp), ("phys_counts", _vp),
+                ("phys_offsets", _vp), ("rank_counts", _vp), ("rank_offsets", _vp), ("row_to_token", _vp),
+                ("slot_to_row", _vp), ("phys_ids", _vp), ("stats", _vp), ("phys_to_logical", _vp),
+                ("phys_rank", _vp), ("replica_count", _vp), ("logical_to_phys", _vp), ("l2p_cols", _i32),
+                ("hot", _vp), ("rank_load", _vp), ("x_q", _vp), ("x_scales", _vp), ("out", _vp),
+                ("out_rounded", _vp), ("seconds", _vp)]
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _stats(v):
+    return {"max_rank": int(v[0]), "mean_rank": float(v[1]), "max_over_mean": float(v[2]),
+            "balancedness": float(v[3]), "max_expert": int(v[4]), "n_active_experts": int(v[5])}
+
+
+class CppOracle:
+    """One loaded copy of the C++ oracle (the default build, or a planted variant)."""
+
+    def __init__(self, path: str | None = None):
+        self.path = path or _build.build()
+        L = self.lib = C.CDLL(self.path)
+        sig = {
+            "orc_threads_default": (_i32, []),
+            "orc_plant": (_i32, []),
+            "orc_route": (_i32, [_f32p, _i64, _i64, _i32, _vp, _i32p, _f64p]),
+            "orc_route_softmax_then_renorm": (_i32, [_f32p, _i64, _i64, _i32, _i32p, _f64p]),
+            "orc_rank_stats": (None, [_i64p, _i32, _i64, _f64p]),
+            "orc_base_rank_counts": (_i32, [_i64p, _i64, _i32, _i32, _i64p]),
+            "orc_eplb_map": (_i32, [_i64p, _i64, _i32, _i32, _i32, _i32p, _i32p, _i32p, _i32p, _i32p]),
+            "orc_eplb_balanced_map": (_i32, [_i64p, _i64, _i32, _i32, _i32p, _i32p, _i32p, _i32p, _f64p]),
+            "orc_eplb_window_sum": (_i32, [_i64p, _i64, _i64, _i64, _i64p]),
+            "orc_dispatch_layout": (_i32, [_i32p, _i64, _i32, _i64, _i32, _i64, _vp, _i32, _vp, _i32, _i32p, _i64p,
+                                           _i64p, _i64p, _i64p, _i64p, _i32p, _i32p, _f64p]),
+            "orc_round_bf16": (None, [_f64p, _i64, _f64p]),
+            "orc_e4m3_value": (C.c_double, [_i32]),
+            "orc_e4m3_encode": (None, [_f32p, _i64, _u8p]),
+            "orc_quantize_groups": (None, [_f32p, _i64, _i64, _i64, _u8p, _f32p]),
+            "orc_quantize_blocks": (None, [_f32p, _i64, _i64, _i64, _u8p, _f32p]),
+            "orc_dequantize_groups_bf16": (None, [_u8p, _f32p, _i64, _i64, _i64, _f64p]),
+            "orc_dequantize_groups": (None, [_u8p, _f32p, _i64, _i64, _i64, _f64p]),
+            "orc_dequantize_blocks": (None, [_u8p, _f32p, _i64, _i64, _i64, _f64p]),
+            "orc_permute": (None, [_vp, _i64, _i32p, _i64, _vp]),
+            "orc_combine": (None, [_f64p, _i64, _i32p, _f64p, _i64, _i32, _vp, _f64p]),
+            "orc_stored_h": (None, [_f64p, _i64, _i64, _i32]),
+            "orc_stored_y": (None, [_f64p, _i64, _i64, _i32]),
+            "orc_expert_rows": (None, [_f64p, _i64, _i64, _i64, _f64p, _f64p, _f64p, _i32, _f64p, _i32]),
+            "orc_layer_forward": (_i32, [C.POINTER(LayerCfg), _f32p, _vp, _i32, _vp, WEIGHT_FN, _vp, _i64,
+                                         C.POINTER(LayerOut)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        self.plant = int(L.orc_plant())
+        self.threads = int(L.orc_threads_default())
+
+    # ---------------------------------------------------------------- route
+    def _route(self, logits, k, bias):
+        L = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = L.shape
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float64)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        rc = self.lib.orc_route(L, T, E, k, _ptr(b), ids, w)
+        if rc == 1:
+            raise ValueError("non-finite router logit or score")
+        if rc:
+            raise ValueError("need 1 <= k <= E")
+        return ids, w
+
+    def route(self, logits, k):
+        return self._route(logits, k, None)
+
+    def route_selection_bias(self, logits, bias, k):
+        return self._route(logits, k, bias)
+
+    def route_softmax_then_renorm(self, logits, k):
+        L = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = L.shape
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float64)
+        if self.lib.orc_route_softmax_then_renorm(L, T, E, k, ids, w):
+            raise ValueError("bad routing input")
+        return ids, w
+
+    # ---------------------------------------------------------------- statistics and maps
+    def rank_stats(self, rank_counts, total_copies):
+        rc = np.ascontiguousarray(rank_counts, dtype=np.int64)
+        out = np.empty(4)
+        self.lib.orc_rank_stats(rc, rc.size, int(total_copies), out)
+        return {"max_rank": int(out[0]), "mean_rank": float(out[1]), "max_over_mean": float(out[2]),
+                "balancedness": float(out[3])}
+
+    def base_rank_counts(self, expert_counts, R, placement="linear"):
+        c = np.ascontiguousarray(expert_counts, dtype=np.int64)
+        out = np.empty(R, np.int64)
+        if placement not in ("linear", "round_robin"):
+            raise ValueError(f"unknown placement {placement!r}")
+        if self.lib.orc_base_rank_counts(c, c.size, R, int(placement == "round_robin"), out):
+            raise ValueError("experts must divide evenly over ranks")
+        return out
+
+    def linear_rank_counts(self, expert_counts, R):
+        return self.base_rank_counts(expert_counts, R, "linear")
+
+    def round_robin_rank_counts(self, expert_counts, R):
+        return self.base_rank_counts(expert_counts, R, "round_robin")
+
+    def eplb_map(self, logical_counts, R, n_redundant, placement="linear"):
+        c = np.ascontiguousarray(logical_counts, dtype=np.int64)
+        E = c.size
+        if placement not in ("linear", "round_robin"):
+            raise ValueError(f"unknown placement {placement!r}")
+        P = E + n_redundant
+        p2l, prank = np.empty(P, np.int32), np.empty(P, np.int32)
+        repc, l2p, hot = np.empty(E, np.int32), np.empty((E, 2), np.int32), np.empty(max(n_redundant, 1), np.int32)
+        if self.lib.orc_eplb_map(c, E, R, n_redundant, int(placement == "round_robin"), p2l, prank, repc, l2p, hot):
+            raise ValueError("unsupported EPLB geometry")
+        return {"P": P, "phys_to_logical": p2l, "phys_rank": prank, "replica_count": repc,
+                "logical_to_phys": l2p, "hot": hot[:n_redundant]}
+
+    def eplb_balanced_map(self, logical_counts, R, n_redundant):
+        c = np.ascontiguousarray(np.asarray(logical_counts).ravel(), dtype=np.int64)
+        E = c.size
+        P = E + n_redundant
+        p2l, prank = np.empty(P, np.int32), np.empty(P, np.int32)
+        repc, l2p, load = np.empty(E, np.int32), np.empty((E, 1 + n_redundant), np.int32), np.empty(R)
+        if self.lib.orc_eplb_balanced_map(c, E, R, n_redundant, p2l, prank, repc, l2p, load):
+            raise ValueError("physical experts must divide evenly over ranks")
+        return {"P": P, "phys_to_logical": p2l, "phys_rank": prank, "replica_count": repc,
+                "logical_to_phys": l2p, "rank_load": load}
+
+    def eplb_window_sum(self, history, W):
+        h = [np.asarray(c, dtype=np.int64) for c in history]
+        if W < 1 or not h:
+            raise ValueError("need W >= 1 and at least one step")
+        arr = np.ascontiguousarray(np.stack(h), dtype=np.int64)
+        out = np.empty(arr.shape[1], np.int64)
+        self.lib.orc_eplb_window_sum(arr, arr.shape[0], arr.shape[1], W, out)
+        return out
+
+    def dispatch_layout(self, topk_ids, E, R, eplb=None, placement="linear"):
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        T, k = ids.shape
+        P = E if eplb is None else int(eplb["P"])
+        N = T * k
+        l2p = repc = None
+        cols = 0
+        if eplb is not None:
+            l2p = np.ascontiguousarray(eplb["logical_to_phys"], dtype=np.int32)
+            repc = np.ascontiguousarray(eplb["replica_count"], dtype=np.int32)
+            cols = l2p.shape[1]
+        phys = np.empty((T, k), np.int32)
+        lc, pc, po = np.empty(E, np.int64), np.empty(P, np.int64), np.empty(P + 1, np.int64)
+        rc, ro = np.empty(R, np.int64), np.empty(R + 1, np.int64)
+        r2t, s2r, st = np.empty(N, np.int32), np.empty((T, k), np.int32), np.empty(12)
+        if placement not in ("linear", "round_robin"):
+            raise ValueError(f"unknown placement {placement!r}")
+        err = self.lib.orc_dispatch_layout(ids, T, k, E, R, P, _ptr(l2p), cols, _ptr(repc),
+                                           int(placement == "round_robin"), phys, lc, pc, po, rc, ro, r2t, s2r, st)
+        if err == 3:
+            raise ValueError("expert id out of range")
+        if err:
+            raise ValueError("experts must divide evenly over ranks")
+        return {"P": P, "phys_ids": phys, "logical_counts": lc, "phys_counts": pc, "phys_offsets": po,
+                "rank_counts": rc, "rank_offsets": ro, "row_to_token": r2t, "slot_to_row": s2r,
+                "stats_before": _stats(st[:6]), "stats_after": _stats(st[6:])}
+
+    # ---------------------------------------------------------------- number formats
+    def round_bf16(self, v):
+        a = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+        out = np.empty_like(a)
+        self.lib.orc_round_bf16(a.ravel(), a.size, out.ravel())
+        return out
+
+    def e4m3_value(self, code):
+        return float(self.lib.orc_e4m3_value(int(code)))
+
+    def e4m3_encode(self, v):
+        a = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+        out = np.empty(a.shape, np.uint8)
+        self.lib.orc_e4m3_encode(a.ravel(), a.size, out.ravel())
+        return out
+
+    def e4m3_decode(self, codes):
+        tab = np.array([self.e4m3_value(c) for c in range(256)])
+        return tab[np.asarray(codes, dtype=np.uint8)]
+
+    def quantize_groups(self, v, group=128):
+        f = np.ascontiguousarray(v, dtype=np.float32)
+        rows, n = f.shape
+        if n % group:
+            raise ValueError("channel count must be a multiple of the group")
+        q, s = np.empty((rows, n), np.uint8), np.empty((rows, n // group), np.float32)
+        self.lib.orc_quantize_groups(f, rows, n, group, q, s)
+        return q, s
+
+    def quantize_blocks(self, w, block=128):
+        f = np.ascontiguousarray(w, dtype=np.float32)
+        r, c = f.shape
+        if r % block or c % block:
+            raise ValueError("matrix must tile by the block")
+        q, s = np.empty((r, c), np.uint8), np.empty((r // block, c // block), np.float32)
+        self.lib.orc_quantize_blocks(f, r, c, block, q, s)
+        return q, s
+
+    def dequantize_groups(self, codes, scales, group=128):
+        q = np.ascontiguousarray(codes, dtype=np.uint8)
+        rows, n = q.shape
+        out = np.empty((rows, n))
+        self.lib.orc_dequantize_groups(q, np.ascontiguousarray(scales, dtype=np.float32), rows, n, group, out)
+        return out
+
+    def dequantize_groups_bf16(self, codes, scales, group=128):
+        q = np.ascontiguousarray(codes, dtype=np.uint8)
+        rows, n = q.shape
+        out = np.empty((rows, n))
+        self.lib.orc_dequantize_groups_bf16(q, np.ascontiguousarray(scales, dtype=np.float32), rows, n, group, out)
+        return out
+
+    def dequantize_blocks(self, codes, scales, block=128):
+        q = np.ascontiguousarray(codes, dtype=np.uint8)
+        r, c = q.shape
+        out = np.empty((r, c))
+        self.lib.orc_dequantize_blocks(q, np.ascontiguousarray(scales, dtype=np.float32), r, c, block, out)
+        return out
+
+    # ---------------------------------------------------------------- permute / FFN / combine
+    def permute(self, x, row_to_token):
+        xa = np.ascontiguousarray(x)
+        r2t = np.ascontiguousarray(row_to_token, dtype=np.int32)
+        if r2t.size and (r2t.min() < 0 or r2t.max() >= xa.shape[0]):
+            raise ValueError("row_to_token out of range")
+        out = np.empty((r2t.size,) + xa.shape[1:], dtype=xa.dtype)
+        row_bytes = xa.strides[0] if xa.ndim > 1 else xa.itemsize
+        self.lib.orc_permute(_ptr(xa), row_bytes, r2t, r2t.size, _ptr(out))
+        return out
+
+    def combine(self, y_rows, slot_to_row, topk_w, shared=None):
+        y = np.ascontiguousarray(y_rows, dtype=np.float64)
+        s2r = np.ascontiguousarray(slot_to_row, dtype=np.int32)
+        w = np.ascontiguousarray(topk_w, dtype=np.float64)
+        T, k = s2r.shape
+        sh = None if shared is None else np.ascontiguousarray(shared, dtype=np.float64)
+        out = np.empty((T, y.shape[1]))
+        self.lib.orc_combine(y, y.shape[1], s2r, w, T, k, _ptr(sh), out)
+        return out
+
+    def stored_h(self, h, mode):
+        a = np.array(h, dtype=np.float64, order="C")
+        self.lib.orc_stored_h(a, a.shape[0], a.shape[1], _MODE[mode])
+        return a
+
+    def stored_y(self, y, mode):
+        a = np.array(y, dtype=np.float64, order="C")
+        self.lib.orc_stored_y(a, a.shape[0], a.shape[1], _MODE[mode])
+        return a
+
+    def swiglu_expert(self, x64, wg64, wu64, wd64, mode):
+        x = np.ascontiguousarray(x64, dtype=np.float64)
+        wg, wu, wd = (np.ascontiguousarray(a, dtype=np.float64) for a in (wg64, wu64, wd64))
+        n, d = x.shape
+        I = wg.shape[1]
+        y = np.empty((n, d))
+        self.lib.orc_expert_rows(x, n, d, I, wg, wu, wd, _MODE[mode], y, self.threads)
+        return y
+
+    # ---------------------------------------------------------------- whole layer
+    def layer_forward(self, cfg, logits, x, weight, tokens=None, eplb_enabled=None, selection_bias=None,
+                      threads=None):
+        """The layer forward of the C++ oracle, with the arguments and result of the
+        numpy oracle's layer_forward, plus "seconds": the C++ steady_clock time of
+        route, layout (with the map), permute, expert FFN, combine, and of fetching
+        the weights through `weight` (not part of the steps)."""
+        T, d, E, k, I, R = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R
+        if eplb_enabled is None:
+            eplb_enabled = cfg.n_redundant > 0
+        balanced = bool(eplb_enabled and getattr(cfg, "eplb_placement", 0) == 1)
+        rr = getattr(cfg, "expert_placement", 0) == 1
+        n_red = cfg.n_redundant if eplb_enabled else 0
+        P = E + n_red
+        mapped = eplb_enabled or rr
+        mode = _MODE[cfg.dtype]
+        fp8d = int(mode == 1 and getattr(cfg, "fp8_dispatch", 0) == 1)
+        c = LayerCfg(T, d, E, I, k, R, int(bool(cfg.shared)), cfg.n_redundant, mode, int(bool(eplb_enabled)),
+                     int(balanced), int(rr), fp8d, int(threads or self.threads))
+        tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+        if tok.size and (np.any(np.diff(tok) <= 0) or tok[0] < 0 or tok[-1] >= T):
+            raise ValueError("tokens must be ascending, distinct and in range")
+        n = tok.size
+        N = T * k
+        a = {"topk_ids": np.empty((T, k), np.int32), "topk_w": np.empty((T, k)),
+             "logical_counts": np.empty(E, np.int64), "phys_counts": np.empty(P, np.int64),
+             "phys_offsets": np.empty(P + 1, np.int64), "rank_counts": np.empty(R, np.int64),
+             "rank_offsets": np.empty(R + 1, np.int64), "row_to_token": np.empty(N, np.int32),
+             "slot_to_row": np.empty((T, k), np.int32), "phys_ids": np.empty((T, k), np.int32),
+             "stats": np.empty(12), "phys_to_logical": np.empty(P, np.int32), "phys_rank": np.empty(P, np.int32),
+             "replica_count": np.empty(E, np.int32),
+             "logical_to_phys": np.empty((E, 1 + n_red if balanced else 2), np.int32),
+             "hot": np.empty(max(n_red, 1), np.int32), "rank_load": np.empty(R),
+             "out": np.empty((n, d)), "out_rounded": np.empty((n, d)), "seconds": np.zeros(6)}
+        quant = mode == 2 or fp8d == 1
+        if quant:
+            a["x_q"], a["x_scales"] = np.empty((n, d), np.uint8), np.empty((n, d // 128), np.float32)
+        o = LayerOut(*[_ptr(a.get(f)) if f != "l2p_cols" else a["logical_to_phys"].shape[1]
+                       for f, _ in LayerOut._fields_])
+        lg = np.ascontiguousarray(logits, dtype=np.float32)
+        xin = np.asarray(x)
+        x_is_f32 = int(xin.dtype != np.uint16)
+        xin = np.ascontiguousarray(xin, dtype=np.float32 if x_is_f32 else np.uint16)
+        sb = None if selection_bias is None else np.ascontiguousarray(selection_bias, dtype=np.float32)
+        keep = {}
+
+        def fetch(which, e, is_f32):
+            m = np.asarray(weight(_WHICH[which], int(e)))
+            f32 = m.dtype != np.uint16
+            m = np.ascontiguousarray(m, dtype=np.float32 if f32 else np.uint16)
+            if len(keep) >= 6:
+                keep.clear()
+            keep[(which, e)] = m
+            is_f32[0] = int(f32)
+            return m.ctypes.data
+
+        cb = WEIGHT_FN(fetch)
+        rc = self.lib.orc_layer_forward(C.byref(c), lg, xin.ctypes.data_as(C.c_void_p), x_is_f32, _ptr(sb), cb,
+                                        tok.ctypes.data_as(C.c_void_p), n, C.byref(o))
+        if rc == 1:
+            raise ValueError("non-finite router logit or score")
+        if rc == 3:
+            raise ValueError("expert id out of range")
+        if rc:
+            raise ValueError(f"C++ oracle layer_forward failed ({rc})")
+        emap = None
+        if balanced:
+            emap = {"P": P, "phys_to_logical": a["phys_to_logical"], "phys_rank": a["phys_rank"],
+                    "replica_count": a["replica_count"], "logical_to_phys": a["logical_to_phys"],
+                    "rank_load": a["rank_load"]}
+        elif mapped:
+            emap = {"P": P, "phys_to_logical": a["phys_to_logical"], "phys_rank": a["phys_rank"],
+                    "replica_count": a["replica_count"], "logical_to_phys": a["logical_to_phys"],
+                    "hot": a["hot"][:n_red]}
+        lay = {"P": P, "phys_ids": a["phys_ids"], "logical_counts": a["logical_counts"],
+               "phys_counts": a["phys_counts"], "phys_offsets": a["phys_offsets"], "rank_counts": a["rank_counts"],
+               "rank_offsets": a["rank_offsets"], "row_to_token": a["row_to_token"], "slot_to_row": a["slot_to_row"],
+               "stats_before": _stats(a["stats"][:6]), "stats_after": _stats(a["stats"][6:])}
+        res = {"topk_ids": a["topk_ids"], "topk_w": a["topk_w"], "layout": lay, "eplb": emap, "tokens": tok,
+               "out": a["out"], "out_rounded": a["out_rounded"],
+               "seconds": dict(zip(("route", "layout", "permute", "expert_ffn", "combine", "weight_fetch"),
+                                   a["seconds"].tolist()))}
+        if quant:
+            res["x_q"], res["x_scales"] = a["x_q"], a["x_scales"]
+        return res
+
+
+_default: CppOracle | None = None
+
+
+def default() -> CppOracle:
+    global _default
+    if _default is None:
+        _default = CppOracle()
+    return _default
+
+
+def __getattr__(name):
+    # module-level access (cpp_oracle.route, ...) goes to the default build
+    if name.startswith("__"):
+        raise AttributeError(name)
+    return getattr(default(), name)

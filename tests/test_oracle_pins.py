@@ -9,10 +9,20 @@ import numpy as np
 import pytest
 import torch
 
+import sys
+
+import _oracles
 import moe_inputs as mi
 from oracle import moe_oracle as O
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(params=_oracles.NAMES, autouse=True)
+def oracle_impl(request, monkeypatch):
+    """Every pin runs against both oracles: the numpy statement and the C++ one."""
+    monkeypatch.setattr(sys.modules[__name__], "O", _oracles.get(request.param))
+    return request.param
 
 
 def load(name):
@@ -675,8 +685,11 @@ def test_fp8_mode_rounds_y_to_bf16():
 
 
 # ------------------------------------------------------------------ planted mistakes
-def test_pins_catch_planted_mistakes(monkeypatch):
-    """Plant plausible slips in the oracle and check that a pin above fails."""
+def test_pins_catch_planted_mistakes(monkeypatch, oracle_impl):
+    """Plant plausible slips in the numpy oracle and check that a pin above fails
+    (the C++ oracle's planted slips are compiled variants: test_oracle_cpp.py)."""
+    if oracle_impl != "numpy":
+        pytest.skip("monkeypatched slips are for the numpy oracle")
     cfg = mi.config(0).scaled(E=1, k=1, R=1)
     x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 9)

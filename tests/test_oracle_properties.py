@@ -8,7 +8,7 @@ import pytest
 from hypothesis import given, settings
 from hypothesis import strategies as st
 
-from oracle import moe_oracle as O
+import _oracles
 
 TIE_VALUES = [-2.0, -0.0, 0.0, 0.5, 0.5, 1.0, 3.0]
 
@@ -33,9 +33,11 @@ def dominating_subset(row, k):
     return found[0]
 
 
+@pytest.mark.parametrize("impl", _oracles.NAMES)
 @settings(max_examples=150, deadline=None)
 @given(routing_case())
-def test_route_matches_brute_force_with_ties(case):
+def test_route_matches_brute_force_with_ties(impl, case):
+    O = _oracles.get(impl)
     logits, k = case
     ids, w = O.route(logits, k)
     for t in range(logits.shape[0]):
@@ -60,9 +62,11 @@ def layout_case(draw):
     return ids, E, R, n_red, placement
 
 
+@pytest.mark.parametrize("impl", _oracles.NAMES)
 @settings(max_examples=150, deadline=None)
 @given(layout_case())
-def test_layout_is_the_stable_sort_by_physical_expert(case):
+def test_layout_is_the_stable_sort_by_physical_expert(impl, case):
+    O = _oracles.get(impl)
     ids, E, R, n_red, placement = case
     T, k = ids.shape
     counts = np.bincount(ids.ravel(), minlength=E)
