@@ -509,21 +509,30 @@ size_t dispatch_ws_bytes(int64_t T, int32_t k, int64_t P) {
   return align_up((size_t)(chunks * P) * 4, 256) + align_up((size_t)N * 4, 256);
 }
 
+// The size checks of a dispatch layout, before anything is computed from the sizes
+// (T * k is formed only once it cannot overflow).
+moe_status_t dispatch_shape_status(int64_t T, int32_t k, int64_t E, int32_t R, const moe_eplb_t *eplb) {
+  const int64_t P = eplb ? eplb->P : E;
+  if (T < 0 || k < 1 || E < 1 || E > 1024 || R < 1 || P < E || P > kMaxP || P % R || E % R)
+    return MOE_ERR_INVALID_ARG;
+  if (eplb && eplb->base_placement != 0 && eplb->base_placement != 1) return MOE_ERR_INVALID_ARG;
+  if (T > (INT32_MAX / 2) / k) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 moe_status_t dispatch_layout(const int32_t *topk_ids, int64_t T, int32_t k, int64_t E, int32_t R,
                              const moe_eplb_t *eplb, int32_t *logical_counts, int32_t *phys_counts,
                              int32_t *phys_offsets, int32_t *rank_counts, int32_t *rank_offsets,
                              int32_t *row_to_token, int32_t *slot_to_row, moe_load_stats_t *stats, void *ws,
                              size_t ws_bytes, int32_t *err, cudaStream_t st) {
+  const moe_status_t shape = dispatch_shape_status(T, k, E, R, eplb);
+  if (shape != MOE_OK) return shape;
   const int64_t P = eplb ? eplb->P : E;
-  if (T < 0 || k < 1 || E < 1 || E > 1024 || R < 1 || P < E || P > kMaxP || P % R || E % R)
-    return MOE_ERR_INVALID_ARG;
   if (!logical_counts || !phys_counts || !phys_offsets || !rank_counts || !rank_offsets)
     return MOE_ERR_INVALID_ARG;
   if (eplb && (!eplb->phys_to_logical || !eplb->replica_count || !eplb->logical_to_phys))
     return MOE_ERR_INVALID_ARG;
-  if (eplb && eplb->base_placement != 0 && eplb->base_placement != 1) return MOE_ERR_INVALID_ARG;
   const int64_t N = T * k;
-  if (N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if (N > 0 && (!topk_ids || !row_to_token || !slot_to_row)) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < dispatch_ws_bytes(T, k, P) || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
   const int chunks = (int)((N + kChunk - 1) / kChunk);
@@ -621,7 +630,7 @@ moe_status_t eplb_balanced_map(const int32_t *logical_counts, int64_t E, int32_t
 }  // namespace moe
 
 MOE_API size_t moe_dispatch_workspace_size(int64_t T, int32_t k, int64_t P) {
-  if (T < 0 || k < 1 || P < 1) return 0;
+  if (T < 0 || k < 1 || P < 1 || T > (INT32_MAX / 2) / k) return 0;
   return moe::dispatch_ws_bytes(T, k, P);
 }
 

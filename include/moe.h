@@ -18,7 +18,10 @@
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers owned by the caller; they must stay
  *     valid until the work queued on `stream` has finished.  The library never
- *     allocates, frees or keeps device memory between calls.  Struct arguments
+ *     allocates or frees device memory, and keeps none between calls, with one
+ *     exception: the scratch array built into the library for
+ *     moe_dispatch_layout_static (MOE_DISPATCH_STATIC_SCRATCH_BYTES on every GPU
+ *     that loads it, until the process exits).  Struct arguments
  *     (moe_shape_t, moe_weights_t, moe_eplb_t, moe_layer_aux_t) are HOST structs
  *     read during the call; the pointers inside them are device pointers.
  *   - Tensors are dense and row-major.  bf16 is stored as uint16 bit patterns,
@@ -29,8 +32,10 @@
  *     range, a pipeline wait that ran out) are OR-ed as MOE_DEV_* bits into the
  *     caller's device word `err` (int32, may be NULL to ignore them); the caller
  *     reads it after synchronising.  Kernels never trap.
- *   - The library holds no global state; calls on different streams may run
- *     concurrently when they share no output buffer.
+ *   - Apart from that array (and its device address, looked up once per device
+ *     and context), the library holds no global state: calls on different streams
+ *     may run concurrently when they share no output buffer.  Calls of
+ *     moe_dispatch_layout_static share the array, so they must not overlap.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -214,7 +219,9 @@ moe_status_t moe_route_biased(const float *logits, const float *selection_bias,
  *     overlaps on a GPU (different streams or host threads) race on it and give
  *     wrong results: keep them on one stream or synchronise in between.
  *   - The first call on each device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture. */
+ *     array's device address, and so does the first call after the device's
+ *     context has changed (a cudaDeviceReset gives the device a new context);
+ *     make those calls before any stream capture. */
 moe_status_t moe_dispatch_layout_static(const int32_t *topk_ids, int64_t T, int32_t k,
                                         int64_t E, int32_t R, const moe_eplb_t *eplb,
                                         int32_t *logical_counts, int32_t *phys_counts,

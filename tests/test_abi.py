@@ -78,6 +78,24 @@ def test_host_validation_without_gpu(lib):
                                  fake, 16, None, None) == 3
 
 
+def test_static_layout_answers_bad_sizes_like_the_workspace_layout(lib):
+    # the built-in-scratch layout checks the sizes first, so a bad size gets the same
+    # status from both entry points (and no size is computed from an overflowing T * k)
+    L = moe.lib()
+    fake = ctypes.c_void_p(256)
+    outs = [fake] * 7
+    for T, k, E, R, want in ((64, 2, 2000, 4, 1),        # E > 1024
+                             (64, 2, 8, 3, 1),           # E % R
+                             (-1, 2, 8, 4, 1),           # T < 0
+                             (64, 0, 8, 4, 1),           # k < 1
+                             (2 ** 40, 8, 256, 32, 2),   # T * k beyond the layout's int32 rows
+                             (2 ** 62, 8, 256, 32, 2)):  # T * k would overflow int64
+        ws_status = L.moe_dispatch_layout(fake, T, k, E, R, None, *outs, None, fake, 1 << 20, None, None)
+        st_status = L.moe_dispatch_layout_static(fake, T, k, E, R, None, *outs, None, None, None)
+        assert ws_status == st_status == want, (T, k, E, R, ws_status, st_status)
+    assert L.moe_dispatch_workspace_size(2 ** 62, 8, 256) == 0
+
+
 def test_layer_workspace_sizes(lib):
     import moe_inputs as mi
     for cfg in mi.CONFIGS:
