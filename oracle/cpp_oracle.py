@@ -26,6 +26,8 @@ _i32, _i64 = C.c_int32, C.c_int64
 WEIGHT_FN = C.CFUNCTYPE(C.c_void_p, C.c_int32, C.c_int32, C.POINTER(C.c_int32))
 _WHICH = ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
 _MODE = {"fp32": 0, "bf16": 1, "fp8": 2}
+# the timed parts of layer_forward, in the order the C++ oracle reports them
+STEPS = ("route", "layout", "permute", "expert_ffn", "combine", "weight_fetch", "weight_prep")
 
 
 class LayerCfg(C.Structure):
@@ -40,7 +42,7 @@ class LayerOut(C.Structure):
                 ("slot_to_row", _vp), ("phys_ids", _vp), ("stats", _vp), ("phys_to_logical", _vp),
                 ("phys_rank", _vp), ("replica_count", _vp), ("logical_to_phys", _vp), ("l2p_cols", _i32),
                 ("hot", _vp), ("rank_load", _vp), ("x_q", _vp), ("x_scales", _vp), ("out", _vp),
-                ("out_rounded", _vp), ("seconds", _vp)]
+                ("out_rounded", _vp), ("out_lo", _vp), ("out_hi", _vp), ("seconds", _vp)]
 
 
 def _ptr(a):
@@ -71,6 +73,7 @@ class CppOracle:
             "orc_dispatch_layout": (_i32, [_i32p, _i64, _i32, _i64, _i32, _i64, _vp, _i32, _vp, _i32, _i32p, _i64p,
                                            _i64p, _i64p, _i64p, _i64p, _i32p, _i32p, _f64p]),
             "orc_round_bf16": (None, [_f64p, _i64, _f64p]),
+            "orc_bf16_bracket": (None, [_f64p, _i64, _f64p, _f64p]),
             "orc_e4m3_value": (C.c_double, [_i32]),
             "orc_e4m3_encode": (None, [_f32p, _i64, _u8p]),
             "orc_quantize_groups": (None, [_f32p, _i64, _i64, _i64, _u8p, _f32p]),
@@ -91,7 +94,11 @@ class CppOracle:
             fn.restype = res
             fn.argtypes = args
         self.plant = int(L.orc_plant())
-        self.threads = int(L.orc_threads_default())
+        # one worker per core this process may run on (the machine may have more)
+        try:
+            self.threads = len(os.sched_getaffinity(0))
+        except (AttributeError, OSError):
+            self.threads = int(L.orc_threads_default())
 
     # ---------------------------------------------------------------- route
     def _route(self, logits, k, bias):
@@ -212,6 +219,12 @@ class CppOracle:
         self.lib.orc_round_bf16(a.ravel(), a.size, out.ravel())
         return out
 
+    def bf16_bracket(self, v):
+        a = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+        lo, hi = np.empty_like(a), np.empty_like(a)
+        self.lib.orc_bf16_bracket(a.ravel(), a.size, lo.ravel(), hi.ravel())
+        return lo, hi
+
     def e4m3_value(self, code):
         return float(self.lib.orc_e4m3_value(int(code)))
 
@@ -309,8 +322,9 @@ class CppOracle:
                       threads=None):
         """The layer forward of the C++ oracle, with the arguments and result of the
         numpy oracle's layer_forward, plus "seconds": the C++ steady_clock time of
-        route, layout (with the map), permute, expert FFN, combine, and of fetching
-        the weights through `weight` (not part of the steps)."""
+        route, layout (with the map), permute, the expert FFN rows, combine, of
+        fetching the weights through `weight`, and of preparing them (float64
+        conversion; block quantisation for the fp8 workload), keyed by STEPS."""
         T, d, E, k, I, R = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.R
         if eplb_enabled is None:
             eplb_enabled = cfg.n_redundant > 0
@@ -337,7 +351,8 @@ class CppOracle:
              "replica_count": np.empty(E, np.int32),
              "logical_to_phys": np.empty((E, 1 + n_red if balanced else 2), np.int32),
              "hot": np.empty(max(n_red, 1), np.int32), "rank_load": np.empty(R),
-             "out": np.empty((n, d)), "out_rounded": np.empty((n, d)), "seconds": np.zeros(6)}
+             "out": np.empty((n, d)), "out_rounded": np.empty((n, d)), "out_lo": np.empty((n, d)),
+             "out_hi": np.empty((n, d)), "seconds": np.zeros(7)}
         quant = mode == 2 or fp8d == 1
         if quant:
             a["x_q"], a["x_scales"] = np.empty((n, d), np.uint8), np.empty((n, d // 128), np.float32)
@@ -383,9 +398,8 @@ class CppOracle:
                "rank_offsets": a["rank_offsets"], "row_to_token": a["row_to_token"], "slot_to_row": a["slot_to_row"],
                "stats_before": _stats(a["stats"][:6]), "stats_after": _stats(a["stats"][6:])}
         res = {"topk_ids": a["topk_ids"], "topk_w": a["topk_w"], "layout": lay, "eplb": emap, "tokens": tok,
-               "out": a["out"], "out_rounded": a["out_rounded"],
-               "seconds": dict(zip(("route", "layout", "permute", "expert_ffn", "combine", "weight_fetch"),
-                                   a["seconds"].tolist()))}
+               "out": a["out"], "out_rounded": a["out_rounded"], "out_lo": a["out_lo"], "out_hi": a["out_hi"],
+               "seconds": dict(zip(STEPS, a["seconds"].tolist()))}
         if quant:
             res["x_q"], res["x_scales"] = a["x_q"], a["x_scales"]
         return res

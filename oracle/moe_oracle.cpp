@@ -101,6 +101,29 @@ float round_to_bf16(float f) {
 double bf16_value(double v) { return (double)round_to_bf16((float)v); }
 double bf16_bits_value(uint16_t b) { return (double)f32_of_bits((uint32_t)b << 16); }
 
+// The bfloat16 value next above r (r itself a bfloat16 value).
+double bf16_next_up(float r) {
+  if (r == 0.f) return (double)f32_of_bits(0x00010000u);
+  const uint32_t u = bits_of_f32(r);
+  return (double)f32_of_bits(r > 0.f ? u + 0x10000u : u - 0x10000u);
+}
+
+// The two bfloat16 values around v: lo <= v <= hi (equal when v is one).  Either is
+// a correct rounding of v by a computation whose own value of v may lie on the other
+// side of the midpoint between them.
+void bf16_bracket(double v, double *lo, double *hi) {
+  const double r = bf16_value(v);
+  if (r == v) {
+    *lo = *hi = r;
+  } else if (r < v) {
+    *lo = r;
+    *hi = bf16_next_up((float)r);
+  } else {
+    *hi = r;
+    *lo = -bf16_next_up(-(float)r);
+  }
+}
+
 // OCP FP8 E4M3 ("fn"): sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
 // field 0 holds the subnormals m/8 * 2^-6; 0x7F and 0xFF are NaN; no infinities.
 double e4m3_value(int code) {
@@ -413,7 +436,7 @@ void stored_y(double *y, int64_t n, int64_t d, int mode) {
 // h = silu(g) * u, y = stored_h(h) W_down (I x d), then stored_y.  Every dot product
 // sums in index order in float64; threads take (4-row block, 256-column block) units.
 void expert_rows(const double *x, int64_t n, int64_t d, int64_t I, const double *wg, const double *wu,
-                 const double *wd, int mode, double *y, int threads) {
+                 const double *wd, int mode, double *y, int threads, double *y_exact = nullptr) {
   constexpr int64_t RB = 4, CB = 256;
   std::vector<double> h(n * I);
   const int64_t nrb = (n + RB - 1) / RB, ncb_i = (I + CB - 1) / CB, ncb_d = (d + CB - 1) / CB;
@@ -452,6 +475,7 @@ void expert_rows(const double *x, int64_t n, int64_t d, int64_t I, const double 
     for (int64_t r = r0; r < r1; ++r)
       for (int64_t i = c0; i < c1; ++i) y[r * d + i] = acc[r - r0][i - c0];
   });
+  if (y_exact) std::copy(y, y + n * d, y_exact);
   stored_y(y, n, d, mode);
 }
 
@@ -519,7 +543,11 @@ struct orc_layer_out {
   float *x_scales;      // [n_tok, d/128]
   double *out;          // [n_tok, d], before the output rounding
   double *out_rounded;  // [n_tok, d]
-  double *seconds;      // [6]: route, layout (with the map), permute, expert FFN, combine, weight fetch
+  double *out_lo;       // [n_tok, d] or NULL: out with every bf16-stored y at the bf16
+  double *out_hi;       //   value just below / above its exact value (bf16 and fp8 modes)
+  double *seconds;      // [7]: route, layout (with the map), permute, expert FFN rows, combine,
+                        //      weight fetch (the caller's callback), weight preparation (to float64,
+                        //      with the block quantisation of the fp8 workload)
 };
 
 int orc_threads_default(void) {
@@ -570,6 +598,9 @@ int orc_dispatch_layout(const int32_t *ids, int64_t T, int32_t k, int64_t E, int
   Layout L{logical_counts, phys_counts, phys_offsets, rank_counts, rank_offsets, row_to_token, slot_to_row, phys_ids,
            stats};
   return dispatch_layout(ids, T, k, E, R, P, l2p, l2p_cols, repc, placement, L);
+}
+void orc_bf16_bracket(const double *v, int64_t n, double *lo, double *hi) {
+  for (int64_t i = 0; i < n; ++i) bf16_bracket(v[i], lo + i, hi + i);
 }
 void orc_round_bf16(const double *v, int64_t n, double *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = bf16_value(v[i]);
@@ -640,7 +671,7 @@ int orc_layer_forward(const orc_layer_cfg *cfg, const float *logits, const void 
   const int k = cfg->k, R = cfg->R, mode = cfg->mode;
   const int threads = cfg->threads > 0 ? cfg->threads : orc_threads_default();
   const int64_t N = T * k;
-  for (int i = 0; i < 6; ++i) o->seconds[i] = 0.0;
+  for (int i = 0; i < 7; ++i) o->seconds[i] = 0.0;
   if (d % 128 && (mode == 2 || cfg->fp8_dispatch)) return 2;
 
   // -------- route
@@ -731,7 +762,8 @@ int orc_layer_forward(const orc_layer_cfg *cfg, const float *logits, const void 
   o->seconds[2] = seconds_since(t0);
 
   // -------- expert FFN: each logical expert over the rows of all its physical replicas
-  std::vector<double> y_perm(M * d);
+  const bool bracket = o->out_lo && o->out_hi;
+  std::vector<double> y_perm(M * d), y_perm_exact(bracket ? M * d : 0);
   std::vector<std::vector<int64_t>> rows_of(E);
   {
     // physical id of each layout row, from the offsets
@@ -744,9 +776,9 @@ int orc_layer_forward(const orc_layer_cfg *cfg, const float *logits, const void 
     }
   }
   std::vector<double> wg(d * I), wu(d * I), wd(I * d);
-  double fetch = 0.0, ffn = 0.0;
+  double fetch = 0.0, prep = 0.0, ffn = 0.0;
   auto run_expert = [&](int which0, int64_t e, const std::vector<int64_t> &idx, const double *src_rows,
-                        bool gathered, std::vector<double> &dst) -> bool {
+                        bool gathered, std::vector<double> &dst, std::vector<double> &dst_exact) -> bool {
     auto tf = clock::now();
     int32_t fg = 0, fu = 0, fd = 0;
     const void *pg = weight(which0, (int32_t)e, &fg);
@@ -754,32 +786,40 @@ int orc_layer_forward(const orc_layer_cfg *cfg, const float *logits, const void 
     const void *pd = weight(which0 + 2, (int32_t)e, &fd);
     fetch += seconds_since(tf);
     if (!pg || !pu || !pd) return false;
-    auto tc = clock::now();
+    auto tp = clock::now();
     weight_values(pg, fg != 0, d, I, mode, wg.data(), threads);
     weight_values(pu, fu != 0, d, I, mode, wu.data(), threads);
     weight_values(pd, fd != 0, I, d, mode, wd.data(), threads);
+    prep += seconds_since(tp);
+    auto tc = clock::now();
     const int64_t n = (int64_t)idx.size();
-    std::vector<double> xin(n * d), yout(n * d);
+    std::vector<double> xin(n * d), yout(n * d), yexact(bracket ? n * d : 0);
     for (int64_t a = 0; a < n; ++a)
       std::copy(src_rows + (gathered ? idx[a] : a) * d, src_rows + (gathered ? idx[a] : a) * d + d, &xin[a * d]);
-    expert_rows(xin.data(), n, d, I, wg.data(), wu.data(), wd.data(), mode, yout.data(), threads);
-    for (int64_t a = 0; a < n; ++a) std::copy(&yout[a * d], &yout[a * d] + d, &dst[(gathered ? idx[a] : a) * d]);
+    expert_rows(xin.data(), n, d, I, wg.data(), wu.data(), wd.data(), mode, yout.data(), threads,
+                bracket ? yexact.data() : nullptr);
+    for (int64_t a = 0; a < n; ++a) {
+      std::copy(&yout[a * d], &yout[a * d] + d, &dst[(gathered ? idx[a] : a) * d]);
+      if (bracket) std::copy(&yexact[a * d], &yexact[a * d] + d, &dst_exact[(gathered ? idx[a] : a) * d]);
+    }
     ffn += seconds_since(tc);
     return true;
   };
   for (int64_t e = 0; e < E; ++e) {
     if (rows_of[e].empty()) continue;
-    if (!run_expert(0, e, rows_of[e], x_perm.data(), true, y_perm)) return 4;
+    if (!run_expert(0, e, rows_of[e], x_perm.data(), true, y_perm, y_perm_exact)) return 4;
   }
-  std::vector<double> shared_y;
-  if (cfg->shared) {
+  std::vector<double> shared_y, shared_y_exact;
+  if (cfg->shared && n_tok > 0) {
     shared_y.assign(n_tok * d, 0.0);
+    shared_y_exact.assign(bracket ? n_tok * d : 0, 0.0);
     std::vector<int64_t> all(n_tok);
     std::iota(all.begin(), all.end(), 0);
-    if (!run_expert(3, 0, all, x_local.data(), false, shared_y)) return 4;
+    if (!run_expert(3, 0, all, x_local.data(), false, shared_y, shared_y_exact)) return 4;
   }
   o->seconds[3] = ffn;
   o->seconds[5] = fetch;
+  o->seconds[6] = prep;
 
   // -------- combine: out[t] = sum_j w[t,j] y[slot_to_row[t,j]] (+ shared), j in order
   t0 = clock::now();
@@ -792,6 +832,26 @@ int orc_layer_forward(const orc_layer_cfg *cfg, const float *logits, const void 
       if (cfg->shared) acc += shared_y[i * d + c];
       o->out[i * d + c] = acc;
       o->out_rounded[i * d + c] = mode == 0 ? acc : bf16_value(acc);
+      if (!bracket) continue;
+      // the same sum with each stored y at the bf16 value below / above its exact
+      // value (the weights are positive)
+      double lo = 0.0, hi = 0.0, a, b;
+      for (int j = 0; j < k; ++j) {
+        const double v = y_perm_exact[compact[o->slot_to_row[t * k + j]] * d + c];
+        if (mode == 0) a = b = v;
+        else bf16_bracket(v, &a, &b);
+        lo += o->topk_w[t * k + j] * a;
+        hi += o->topk_w[t * k + j] * b;
+      }
+      if (cfg->shared) {
+        const double v = shared_y_exact[i * d + c];
+        if (mode == 0) a = b = v;
+        else bf16_bracket(v, &a, &b);
+        lo += a;
+        hi += b;
+      }
+      o->out_lo[i * d + c] = lo;
+      o->out_hi[i * d + c] = hi;
     }
   });
   o->seconds[4] = seconds_since(t0);

@@ -320,6 +320,25 @@ def round_bf16(v) -> np.ndarray:
     return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def _bf16_next_up(r: np.ndarray) -> np.ndarray:
+    """The bfloat16 value next above each bfloat16 value r."""
+    f = np.ascontiguousarray(np.asarray(r, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.int64)
+    u = np.where(f > 0, u + 0x10000, np.where(f < 0, u - 0x10000, 0x00010000))
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def bf16_bracket(v):
+    """The two bfloat16 values around each v: lo <= v <= hi (equal when v is one).
+    A computation whose own value of v lies on the other side of the midpoint
+    between them rounds to the other one; both are correct roundings of v."""
+    v = np.asarray(v, dtype=np.float64)
+    r = round_bf16(v)
+    lo = np.where(r <= v, r, -_bf16_next_up(-r))
+    hi = np.where(r >= v, r, _bf16_next_up(r))
+    return lo, hi
+
+
 def bf16_bits_to_f64(bits) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -440,6 +459,15 @@ def stored_y(y, mode: str):
     return round_bf16(y) if mode in ("bf16", "fp8") else y
 
 
+def swiglu_expert_exact(x64, wg64, wu64, wd64, mode: str):
+    """One expert's FFN before its output is stored: h = silu(x W_gate) * (x W_up),
+    stored as the mode stores it, then y = h W_down in float64."""
+    g = x64 @ wg64
+    u = x64 @ wu64
+    h = stored_h(silu(g) * u, mode)
+    return h @ wd64
+
+
 def swiglu_expert(x64, wg64, wu64, wd64, mode: str):
     """One expert's FFN ("6.4 ...", section 2.1: gate, up, down):
     h = silu(x W_gate) * (x W_up); y = h W_down; float64 matmuls.
@@ -447,10 +475,7 @@ def swiglu_expert(x64, wg64, wu64, wd64, mode: str):
     mode "fp32": no intermediate rounding.  "bf16": h and y rounded to bf16 where the
     kernels store them.  "fp8": h quantised per row per 128 channels (e4m3), y
     rounded to bf16.  (x and the weights arrive already dequantised.)"""
-    g = x64 @ wg64
-    u = x64 @ wu64
-    h = stored_h(silu(g) * u, mode)
-    return stored_y(h @ wd64, mode)
+    return stored_y(swiglu_expert_exact(x64, wg64, wu64, wd64, mode), mode)
 
 
 def combine(y_rows: np.ndarray, slot_to_row: np.ndarray, topk_w: np.ndarray, shared=None):
@@ -529,14 +554,25 @@ def layer_forward(cfg, logits, x, weight, tokens=None, eplb_enabled=None, select
     phys = lay["phys_ids"][tokens]                         # [n, k] physical ids
     p2l = emap["phys_to_logical"] if emap is not None else np.arange(E)
     logical = p2l[phys]
-    y_slots = np.zeros((len(tokens), k, cfg.d))
+    y_exact = np.zeros((len(tokens), k, cfg.d))
     for e in np.unique(logical):
         sel = np.nonzero(logical == e)
-        yv = swiglu_expert(xs[sel[0]], wmat("w_gate", e), wmat("w_up", e), wmat("w_down", e), mode)
-        y_slots[sel[0], sel[1]] = yv
-    out = np.einsum("tj,tjd->td", w[tokens], y_slots)
+        y_exact[sel[0], sel[1]] = swiglu_expert_exact(xs[sel[0]], wmat("w_gate", e), wmat("w_up", e),
+                                                      wmat("w_down", e), mode)
+    y_slots = stored_y(y_exact.reshape(-1, cfg.d), mode).reshape(y_exact.shape)
+    wt = w[tokens]
+    out = np.einsum("tj,tjd->td", wt, y_slots)
+    # the same sum with every stored y at the bf16 value below / above its exact
+    # value: a kernel whose own y lies across a rounding midpoint from the exact one
+    # stores the other neighbour, which is as correct (the weights are positive)
+    lo, hi = (y_exact, y_exact) if mode == "fp32" else bf16_bracket(y_exact)
+    out_lo, out_hi = np.einsum("tj,tjd->td", wt, lo), np.einsum("tj,tjd->td", wt, hi)
     if cfg.shared:
-        out = out + swiglu_expert(x_local, wmat("ws_gate", 0), wmat("ws_up", 0), wmat("ws_down", 0), mode)
+        s_exact = swiglu_expert_exact(x_local, wmat("ws_gate", 0), wmat("ws_up", 0), wmat("ws_down", 0), mode)
+        out = out + stored_y(s_exact, mode)
+        s_lo, s_hi = (s_exact, s_exact) if mode == "fp32" else bf16_bracket(s_exact)
+        out_lo, out_hi = out_lo + s_lo, out_hi + s_hi
     res["out"] = out
     res["out_rounded"] = out if mode == "fp32" else round_bf16(out)
+    res["out_lo"], res["out_hi"] = out_lo, out_hi
     return res

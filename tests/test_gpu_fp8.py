@@ -75,14 +75,15 @@ def run_ffn_fp8(cfg, logits=None, mode=None):
 
 
 SMALL = mi.config(4).scaled(T=300, d=256, E=8, I=256, R=4)
+MODES = ["wide", "pair"]      # one-SM tiles, SM-pair tiles
 
 
-@pytest.mark.parametrize("mode", ["wide", "pair"])
+@pytest.mark.parametrize("mode", MODES)
 def test_ffn_fp8_small(mode):
     run_ffn_fp8(SMALL, mode=mode)
 
 
-@pytest.mark.parametrize("mode", ["wide", "pair"])
+@pytest.mark.parametrize("mode", MODES)
 def test_ffn_fp8_skewed_groups_and_ragged_tiles(mode):
     cfg = SMALL.scaled(T=333, E=16, k=4, d=512, I=384, R=4)
     rng = np.random.default_rng(0)
@@ -92,6 +93,7 @@ def test_ffn_fp8_skewed_groups_and_ragged_tiles(mode):
     run_ffn_fp8(cfg, logits=l, mode=mode)
 
 
-@pytest.mark.parametrize("mode", ["wide", "pair"])
+@pytest.mark.parametrize("mode", MODES)
 def test_ffn_fp8_single_token(mode):
     run_ffn_fp8(SMALL.scaled(T=1), mode=mode)
+

@@ -684,6 +684,48 @@ def test_fp8_mode_rounds_y_to_bf16():
     assert O.swiglu_expert(x, wg, wu, wdm, "fp8")[0, 0] == 1.0
 
 
+# ------------------------------------------------------------------ the bf16 rounding envelope
+def test_bf16_bracket_by_hand():
+    lo, hi = O.bf16_bracket(np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 2.0 ** -9, -3.0 - 2.0 ** -7, 0.0, 1e-45, -2.0]))
+    # bf16-exact values bracket themselves; 1 + 2^-8 (a tie) and 1 + 2^-9 sit between
+    # 1 and 1 + 2^-7; -3 - 2^-7 between -3 - 2^-6 and -3; 1e-45 between 0 and 2^-133
+    assert lo.tolist() == [1.0, 1.0, 1.0, -3.0 - 2.0 ** -6, 0.0, 0.0, -2.0]
+    assert hi.tolist() == [1.0, 1.0 + 2.0 ** -7, 1.0 + 2.0 ** -7, -3.0, 0.0, 2.0 ** -133, -2.0]
+
+
+def test_layer_envelope_holds_the_round_to_nearest_output():
+    for cfg in (mi.config(2).scaled(T=40, d=128, E=8, I=128, R=4), mi.config(0),
+                mi.config(4).scaled(T=40, d=128, E=8, I=128, R=4)):
+        x = mi.make_x(cfg)
+        l = mi.make_logits(cfg)
+        wt = tiny_weights(cfg, 17)
+        res = O.layer_forward(cfg, l, x, wt)
+        assert np.all(res["out_lo"] <= res["out"] + 1e-12) and np.all(res["out"] <= res["out_hi"] + 1e-12)
+        if cfg.dtype == "fp32":            # nothing is rounded: the envelope is the output
+            assert np.allclose(res["out_lo"], res["out"], rtol=0, atol=1e-15)
+            assert np.allclose(res["out_hi"], res["out"], rtol=0, atol=1e-15)
+        else:                              # at most one bf16 step of each y, weighted
+            assert np.all(res["out_hi"] - res["out_lo"] <= 2.0 ** -7 * (np.abs(res["out"]) + 4.0))
+            assert np.any(res["out_hi"] > res["out_lo"])
+
+
+def test_layer_envelope_by_hand():
+    # one token, E = k = 1 with weight 1, d = 1: y = h w_down = 1 + 2^-8 exactly (the
+    # bf16 tie), so the envelope is [1, 1 + 2^-7] and the rounded output 1
+    cfg = mi.config(2).scaled(T=1, d=128, E=1, k=1, I=128, R=1, shared=False, zipf_bias=False)
+    wg = np.zeros((128, 128), np.float32)
+    wu = np.zeros((128, 128), np.float32)
+    wd = np.zeros((128, 128), np.float32)
+    wg[0, 0], wu[0, 0] = 64.0, 2.0 ** -6            # h_0 = silu(64) * 1 = 64 * 2^-6 = 1
+    wd[0, 0] = 1.0 + 2.0 ** -8                       # y_0 = 1 + 2^-8
+    W = {"w_gate": wg, "w_up": wu, "w_down": wd}
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0] = 1.0
+    res = O.layer_forward(cfg, np.zeros((1, 1), np.float32), x, lambda which, e: W[which])
+    assert res["out"][0, 0] == 1.0
+    assert res["out_lo"][0, 0] == 1.0 and res["out_hi"][0, 0] == 1.0 + 2.0 ** -7
+
+
 # ------------------------------------------------------------------ planted mistakes
 def test_pins_catch_planted_mistakes(monkeypatch, oracle_impl):
     """Plant plausible slips in the numpy oracle and check that a pin above fails
@@ -694,15 +736,15 @@ def test_pins_catch_planted_mistakes(monkeypatch, oracle_impl):
     x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 9)
     ref = torch_swiglu(x, wt("w_gate", 0), wt("w_up", 0), wt("w_down", 0)).numpy()
-    real = O.swiglu_expert
+    real = O.swiglu_expert_exact
 
     def swapped(x64, wg, wu, wd, mode):           # gate and up exchanged
         return real(x64, wu, wg, wd, mode)
 
-    monkeypatch.setattr(O, "swiglu_expert", swapped)
+    monkeypatch.setattr(O, "swiglu_expert_exact", swapped)
     out = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)["out"]
     assert not np.allclose(out, ref, rtol=1e-6, atol=1e-6)
-    monkeypatch.setattr(O, "swiglu_expert", real)
+    monkeypatch.setattr(O, "swiglu_expert_exact", real)
 
     monkeypatch.setattr(O, "silu", lambda z: z / (1.0 + np.exp(z)))   # sign slip
     out = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)["out"]
