@@ -11,8 +11,12 @@ launching stream.  L2 is flushed (a 512 MiB write) between timed steps, outside
 the timed spans.  Under torchrun every rank runs its own batch on its own GPU
 (weak scaling, no data-path collective); rank 0 prints one JSON line.
 
---impl reference times the CPU oracle (oracle/, plain float64 numpy) on the host
-cores instead, one token of the same workload per step.
+--impl reference times the C++ float64 CPU oracle (oracle/moe_oracle.cpp) on the
+host cores instead: each step routes and lays out the whole batch and runs the
+rest of the layer for a small strided sample of its tokens.
+
+The default workload is the largest one, prefill_fp8_skew (16384 tokens, e4m3
+experts); --workload decode_bf16 and the others stay available.
 """
 from __future__ import annotations
 
@@ -39,6 +43,7 @@ METRIC = "MoE layer tokens/s on 1 B300; grouped-GEMM % tensor peak; permute GB/s
 # folded into it); tests/test_multirank.py checks them against csrc/layout.cu.
 LAYOUT_CHUNK_SLOTS, SMALL_LAYOUT_EXPERTS, SMALL_ROUTE_WORK = 2048, 512, 16
 UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 7700.0   # B300 HBM3e nominal bandwidth; the measured copy figure is the primary denominator
 
 
 def parse():
@@ -46,9 +51,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode_bf16")
+    ap.add_argument("--workload", default="prefill_fp8_skew")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8, help="tokens in the CPU-baseline sample")
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="tokens in the CPU-baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=2, help="tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--override", action="append", default=[], metavar="FIELD=INT",
                     help="change an integer field of the workload (T, E, R, k, d, I, n_redundant, eplb_placement, "
@@ -397,24 +403,48 @@ def run_ours(args, world, rank, local):
             rec["TFLOP/s"] = round(flops / (ms * 1e9), 1)
         kernels[name] = rec
     kernels["dispatch_layout"] = {"ms": round(float(stage_ms[1]), 5)}
-    gu_ms = float(stage_ms[3])
-    if weight_bound or cfg.dtype == "fp32":
+    gu_ms, dn_ms = float(stage_ms[3]), float(stage_ms[4])
+    tensor_peak = None
+    if not (weight_bound or cfg.dtype == "fp32"):
+        if cfg.dtype == "fp8":
+            tensor_peak = round(fp8_gemm_peak(), 1)
+            pk["source"] = "measured in this run: cuBLAS e4m3 8192^3 (torch._scaled_mm), best of 20"
+        else:
+            tensor_peak = pk["bf16_tflops"]
+    # every kernel against its roofline: the measured peaks, and the HBM-bound steps
+    # also against the nominal HBM3e bandwidth
+    for name, bound in (("expert_gate_up", "gemm"), ("expert_down", "gemm"), ("permute", "hbm"),
+                        ("combine", "hbm"), ("route", "hbm")):
+        rec = kernels[name]
+        if bound == "gemm" and tensor_peak is not None:
+            rec["frac"] = round(rec["TFLOP/s"] / tensor_peak, 4)
+            rec["bound"] = "tensor"
+        else:
+            rec["frac"] = round(rec["GB/s"] / pk["hbm_gbs"], 4)
+            rec["frac_nominal_hbm"] = round(rec["GB/s"] / NOMINAL_HBM_GBS, 4)
+            rec["bound"] = "hbm"
+    if tensor_peak is None:
         ach = gu_bytes / (gu_ms * 1e6)
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4)}
     else:
         ach = gu_flops / (gu_ms * 1e9)
-        if cfg.dtype == "fp8":
-            peak = round(fp8_gemm_peak(), 1)
-            pk["source"] = "measured in this run: cuBLAS e4m3 8192^3 (torch._scaled_mm), best of 20"
-        else:
-            peak = pk["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4)}
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tensor_peak, 4)}
     roof.update({"kernel": "expert_gate_up (grouped GEMM + SwiGLU)", "traffic": traffic_for("expert_gate_up", cfg.name),
                  "peak_source": pk["source"],
                  "algorithmic": (f"{active_logical} active experts x 2*d*I*{sw} B weights + x rows + h rows"
                                  if roof["bound"] == "hbm" else "2*rows*d*2I flops")})
+    # the expert FFN's own roofline, expert by expert: each active expert takes at
+    # least the longer of its FLOPs at the tensor peak and its weight bytes at the
+    # HBM bandwidth, sum_e max(6 n_e d I / peak, 3 d I s_w / BW)
+    lc_h = lc.cpu().numpy().astype(np.int64)
+    n_e = [int(c) for c in lc_h if c > 0] + ([T] if cfg.shared else [])
+    flop_rate = (tensor_peak if tensor_peak is not None else pk["bf16_tflops"]) * 1e12
+    ffn_floor_s = sum(max(6.0 * n * d * I / flop_rate, 3.0 * d * I * sw / (pk["hbm_gbs"] * 1e9)) for n in n_e)
+    expert_ffn = {"ms": round(gu_ms + dn_ms, 5), "roofline_ms": round(ffn_floor_s * 1e3, 5),
+                  "frac": round(ffn_floor_s * 1e3 / (gu_ms + dn_ms), 4),
+                  "rule": "sum over active experts of max(6 n_e d I / tensor peak, 3 d I s_w / HBM copy bandwidth)"}
 
     # ---------------- end to end through moe_layer_forward, host buffers
     h_logits = torch.from_numpy(logits_np).pin_memory()
@@ -504,7 +534,8 @@ def run_ours(args, world, rank, local):
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator)",
-            "config": workload_config(cfg), "roofline": roof, "kernels": kernels, "e2e": e2e,
+            "config": workload_config(cfg), "roofline": roof, "kernels": kernels, "expert_ffn": expert_ffn,
+            "e2e": e2e,
             "gpu_launches": int(layer_launches * args.steps),
             "load": {"max_over_mean_before": round(st[0].max_over_mean, 4),
                      "max_over_mean_after": round(st[1].max_over_mean, 4),
@@ -516,88 +547,59 @@ def run_ours(args, world, rank, local):
 
 
 # ------------------------------------------------------------------ the oracle, timed
-def _affinity_cores():
-    try:
-        return len(os.sched_getaffinity(0))
-    except Exception:
-        return os.cpu_count() or 1
-
-
-def oracle_threads():
-    """Threads numpy's BLAS runs the oracle's matmuls with.  Without threadpoolctl
-    this is OpenBLAS's default: OPENBLAS_NUM_THREADS / OMP_NUM_THREADS, else every
-    core the process may run on."""
-    try:
-        from threadpoolctl import threadpool_info
-        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
-        if n:
-            return max(n)
-    except Exception:
-        pass
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(var, "").isdigit():
-            return int(os.environ[var])
-    return _affinity_cores()
-
-
-class host_cores:
-    """Let the oracle's BLAS calls use every host core while it is timed (the
-    environment may pin BLAS to one thread); its elementwise numpy work stays
-    single-threaded."""
-
-    def __enter__(self):
-        self.ctx = None
-        try:
-            from threadpoolctl import threadpool_limits
-            self.ctx = threadpool_limits(limits=_affinity_cores(), user_api="blas")
-        except Exception:
-            pass
-        return self
-
-    def __exit__(self, *a):
-        if self.ctx is not None:
-            self.ctx.restore_original_limits()
-
-
-def sample_weights(cfg, tokens, logits, dev):
-    """Host copies of the logical weights the sampled tokens touch (drawn by the
-    generator on the device when there is one, else on the host)."""
-    from oracle import moe_oracle as O
-    ids, _ = O.route(logits, cfg.k)
-    need = {(w, int(e)) for t in tokens for e in ids[t] for w in ("w_gate", "w_up", "w_down")}
-    if cfg.n_redundant:
-        need = {(w, e) for w in ("w_gate", "w_up", "w_down") for e in range(cfg.E)} if len(tokens) > 4 else need
-    if cfg.shared:
-        need |= {(w, 0) for w in ("ws_gate", "ws_up", "ws_down")}
-    store = {}
-    for which, e in sorted(need):
+def oracle_weights(cfg, dev):
+    """weight(which, e) for the C++ oracle: the generator's logical matrix, drawn on
+    the device when there is one (else on the host) and copied to host memory.  The
+    oracle asks for each expert once per call; its fetch time is reported apart from
+    the layer's steps (the GPU side holds its weights resident too)."""
+    def weight(which, e):
         if dev is not None:
             import torch
-            t = mi.make_weight_device(cfg, which, e, dev)
-            store[(which, e)] = t.cpu().numpy() if cfg.dtype == "fp32" else t.view(torch.int16).cpu().numpy().view(np.uint16)
-        else:
-            store[(which, e)] = mi.make_weight_host(cfg, which, e)
-    return lambda which, e: store[(which, int(e))]
+            t = mi.make_weight_device(cfg, which, int(e), dev)
+            return t.cpu().numpy() if cfg.dtype == "fp32" else t.view(torch.int16).cpu().numpy().view(np.uint16)
+        return mi.make_weight_host(cfg, which, int(e))
+    return weight
 
 
 def cpu_baseline(cfg, logits, x, n_tokens, dev):
-    from oracle import moe_oracle as O
-    tokens = np.arange(min(n_tokens, cfg.T))
-    weight = sample_weights(cfg, tokens, logits, dev)
-    with host_cores():
-        cores = oracle_threads()
-        t0 = time.perf_counter()
-        O.layer_forward(cfg, logits, x, weight, tokens=tokens)
-        dt = time.perf_counter() - t0
-    return {"value": round(len(tokens) / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{len(tokens)} tokens of {cfg.name} (routing and layout of all {cfg.T} tokens, the expert "
-                      f"FFN and combine of the sample), {dt:.1f} s"}
+    """The C++ float64 oracle (oracle/moe_oracle.cpp) on the host cores: routing and
+    layout of the whole batch, then the permute, expert FFN and combine of a strided
+    sample of n_tokens tokens (every T/n-th), one worker thread per core.  The value
+    is the whole batch's tokens/s projected from the measured parts: routing, layout
+    and the weight preparation of every active expert once (measured per touched
+    expert), plus permute + FFN + combine per token times T."""
+    from oracle import cpp_oracle
+    co = cpp_oracle.default()
+    n = max(1, min(n_tokens, cfg.T))
+    tokens = np.unique(np.linspace(0, cfg.T - 1, n).round().astype(np.int64))
+    t0 = time.perf_counter()
+    r = co.layer_forward(cfg, logits, x, oracle_weights(cfg, dev), tokens=tokens)
+    wall = time.perf_counter() - t0
+    sec = r["seconds"]
+    lay = r["layout"]
+    p2l = r["eplb"]["phys_to_logical"] if r["eplb"] is not None else np.arange(lay["P"])
+    active = len(set(p2l[lay["phys_counts"] > 0].tolist())) + (1 if cfg.shared else 0)
+    touched = len(set(p2l[lay["phys_ids"][tokens].ravel()].tolist())) + (1 if cfg.shared else 0)
+    per_token = (sec["permute"] + sec["expert_ffn"] + sec["combine"]) / len(tokens)
+    whole = sec["route"] + sec["layout"] + sec["weight_prep"] * active / touched + per_token * cfg.T
+    steps = sec["route"] + sec["layout"] + sec["permute"] + sec["expert_ffn"] + sec["combine"] + sec["weight_prep"]
+    return {"value": round(cfg.T / whole, 3), "unit": UNIT, "cores": co.threads, "threads": co.threads,
+            "kind": "oracle",
+            "sample": (f"C++ float64 oracle, {co.threads} threads: routing and layout of all {cfg.T} tokens of "
+                       f"{cfg.name}, permute + expert FFN + combine of {len(tokens)} strided tokens "
+                       f"({touched} of {active} active experts' weights prepared); value = {cfg.T} tokens over the "
+                       f"projected whole-batch time {whole:.1f} s (weight preparation scaled to all active experts, "
+                       f"per-token steps scaled to {cfg.T} tokens); {wall:.1f} s wall"),
+            "sample_tokens_per_s": round(len(tokens) / steps, 3),
+            "seconds": {k: round(v, 4) for k, v in sec.items()},
+            "projected_whole_batch_s": round(whole, 3)}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    from oracle import moe_oracle as O
+    from oracle import cpp_oracle
+    co = cpp_oracle.default()
     cfg = workload(args)
     logits, x = mi.make_logits(cfg), mi.make_x(cfg)
     dev = None
@@ -607,24 +609,38 @@ def run_reference(args, world, rank):
             dev = torch.device("cuda", 0)
     except Exception:
         dev = None
-    pool = np.arange(min(4, cfg.T))          # steps cycle over these tokens
-    weight = sample_weights(cfg, pool, logits, dev)
-    with host_cores():
-        cores = oracle_threads()
-        for i in range(args.warmup):
-            O.layer_forward(cfg, logits, x, weight, tokens=pool[i % len(pool):i % len(pool) + 1])
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            O.layer_forward(cfg, logits, x, weight, tokens=pool[i % len(pool):i % len(pool) + 1])
-        dt = time.perf_counter() - t0
-    value = args.steps / dt
+    weight = oracle_weights(cfg, dev)
+    per_step = max(1, min(args.ref_tokens, cfg.T))
+
+    def step(i):
+        # a different strided sample each step: tokens i, i + T/n, ...
+        stride = max(1, cfg.T // per_step)
+        tokens = np.arange(i % stride, cfg.T, stride)[:per_step]
+        r = co.layer_forward(cfg, logits, x, weight, tokens=tokens)
+        return len(tokens), r["seconds"]
+
+    for i in range(args.warmup):
+        step(i)
+    total = {k: 0.0 for k in cpp_oracle.STEPS}
+    done = 0
+    for i in range(args.steps):
+        n, sec = step(args.warmup + i)
+        done += n
+        for k, v in sec.items():
+            total[k] += v
+    dt = sum(v for k, v in total.items() if k != "weight_fetch")
+    value = done / dt
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator)", "config": workload_config(cfg),
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"one token of {cfg.name} per step (routing and layout of all {cfg.T} "
-                                       f"tokens, that token's expert FFN and combine)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": co.threads, "threads": co.threads,
+                             "kind": "oracle",
+                             "sample": f"C++ float64 oracle, {co.threads} threads; each step: routing and layout of "
+                                       f"all {cfg.T} tokens of {cfg.name}, then permute, expert FFN (weights prepared "
+                                       f"for the experts the sample touches) and combine of {per_step} strided "
+                                       f"tokens; weight fetch from the generator not timed",
+                             "seconds": {k: round(v, 4) for k, v in total.items()}},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
