@@ -385,16 +385,26 @@ __global__ void __launch_bounds__(1024) eplb_map_kernel(const int32_t *__restric
 
 // The page's load-aware placement ("6.4 ...", section 5.2) as a physical-expert map.
 // One CTA of 1024 threads; E <= 1024, P = E + n_red <= 2048, R <= 1024.
-// Loads per replica are count / replicas.  Comparisons between them use exact
-// cross-multiplication, a/b > c/d <=> a*d > c*b: with counts below 2^31 and at most
-// 1025 replicas two different quotients differ by at least 1/1025^2, more than an
-// fp64 ulp of any of them, so the correctly rounded fp64 quotients the page's
-// procedure compares are ordered the same way (and equal only when exactly equal).
-// The per-rank loads are summed in fp64 in the procedure's order, so the map and the
-// loads are exactly the ones it gives.
+// Loads per replica are count / replicas, the correctly rounded fp64 quotients the
+// page's procedure compares; the redundant slots are handed out by comparing them.
+// Ordering the replicas uses exact cross-multiplication, a/b > c/d <=> a*d > c*b:
+// with counts below 2^31 and at most 1025 replicas two different quotients differ
+// by at least 1/1025^2, more than an fp64 ulp of any of them, so the fp64 quotients
+// are ordered the same way (and equal only when exactly equal).  The per-rank loads
+// are summed in fp64 in the procedure's order, so the map and the loads are exactly
+// the ones it gives.
 __device__ __forceinline__ bool heavier(int64_t ca, int ra, int ia, int64_t cb, int rb, int ib) {
   const int64_t l = ca * rb, r = cb * ra;
   return l > r || (l == r && ia < ib);
+}
+
+// Warp-wide argmin of 64-bit keys held one per lane, the lowest `id` on ties; lanes
+// without a candidate pass key = ~0.  Three 32-bit warp reductions.
+__device__ __forceinline__ int warp_argmin64(uint64_t key, int id) {
+  const uint32_t hi = (uint32_t)(key >> 32), lo = (uint32_t)key;
+  const uint32_t mh = __reduce_min_sync(kFull, hi);
+  const uint32_t ml = __reduce_min_sync(kFull, hi == mh ? lo : ~0u);
+  return (int)__reduce_min_sync(kFull, hi == mh && lo == ml ? (uint32_t)id : ~0u);
 }
 
 __global__ void __launch_bounds__(1024) eplb_balanced_kernel(const int32_t *__restrict__ counts, int E, int R,
@@ -411,6 +421,7 @@ __global__ void __launch_bounds__(1024) eplb_balanced_kernel(const int32_t *__re
   for (int e = tid; e < E; e += blockDim.x) {
     cnt[e] = counts[e];
     rep[e] = 1;
+    per[e] = (double)counts[e];
   }
   for (int r = tid; r < R; r += blockDim.x) {
     load[r] = 0.0;
@@ -419,67 +430,122 @@ __global__ void __launch_bounds__(1024) eplb_balanced_kernel(const int32_t *__re
   for (int i = tid; i < E * stride; i += blockDim.x) logical_to_phys[i] = -1;
   __syncthreads();
   // 1. each redundant slot to the expert with the highest load per replica (lowest
-  // index on a tie); one warp, so no block barrier per slot
+  // index on a tie).  One warp: lane l keeps the best of experts l, l + 32, ... (the
+  // float64 loads count / replicas, whose bit patterns order as the values do), a
+  // warp reduction picks the winner, and only the winner's lane looks again.
   if (warp == 0) {
-    for (int it = 0; it < n_red; ++it) {
-      int bi = -1;
-      for (int e = lane; e < E; e += 32)
-        if (bi < 0 || heavier(cnt[e], rep[e], e, cnt[bi], rep[bi], bi)) bi = e;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const int oi = __shfl_xor_sync(kFull, bi, o);
-        if (oi >= 0 && (bi < 0 || heavier(cnt[oi], rep[oi], oi, cnt[bi], rep[bi], bi))) bi = oi;
+    auto lane_best = [&](uint64_t *key, int *id) {
+      *key = ~0ull;
+      *id = -1;
+      for (int e = lane; e < E; e += 32) {
+        const uint64_t k = ~(uint64_t)__double_as_longlong(per[e]);  // larger load -> smaller key
+        if (*id < 0 || k < *key) {
+          *key = k;
+          *id = e;
+        }
       }
-      if (lane == 0) rep[bi] += 1;
+    };
+    uint64_t key;
+    int id;
+    lane_best(&key, &id);
+    for (int it = 0; it < n_red; ++it) {
+      const int bi = warp_argmin64(key, id < 0 ? 0x7fffffff : id);
+      if ((bi & 31) == lane) {
+        rep[bi] += 1;
+        per[bi] = (double)cnt[bi] / (double)rep[bi];
+        lane_best(&key, &id);
+      }
       __syncwarp();
     }
   }
   __syncthreads();
-  // 2. replicas heaviest first; equal loads keep expert order, then replica order
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int64_t ce = cnt[e];
-    const int re = rep[e];
+  // 2. replicas heaviest first; equal loads keep expert order, then replica order.
+  // per[e] now holds count / replicas of every expert; G consecutive threads count the
+  // replicas heavier than expert e's over interleaved parts of the experts.
+  {
+    const int G = E <= 256 ? 4 : (E <= 512 ? 2 : 1);  // threads per expert (1024 threads)
+    const int e = tid / G, part = tid % G;
     int pos = 0;
-    for (int f = 0; f < E; ++f) pos += heavier(cnt[f], rep[f], f, ce, re, e) ? rep[f] : 0;
-    for (int j = 0; j < re; ++j) {
-      oe[pos + j] = (int16_t)e;
-      oj[pos + j] = (int16_t)j;
+    int64_t ce = 0;
+    int re = 0;
+    if (e < E) {
+      ce = cnt[e];
+      re = rep[e];
+      for (int f = part; f < E; f += G) pos += heavier(cnt[f], rep[f], f, ce, re, e) ? rep[f] : 0;
     }
-    replica_count[e] = re;
-    per[e] = (double)ce / (double)re;
+    for (int o = 1; o < G; o <<= 1) pos += __shfl_xor_sync(kFull, pos, o);
+    if (e < E && part == 0) {
+      for (int j = 0; j < re; ++j) {
+        oe[pos + j] = (int16_t)e;
+        oj[pos + j] = (int16_t)j;
+      }
+      replica_count[e] = re;
+    }
   }
   __syncthreads();
   // 3. each replica onto the lightest rank with a free slot (lowest rank on a tie).
-  // The loads are non-negative doubles, whose bit patterns order like the values, so
-  // they are compared as 64-bit integers.
-  if (warp == 0) {
+  // One warp.  With R <= 32 lane r holds rank r's load and used slots in registers; a
+  // warp reduction over the loads' bit patterns (non-negative doubles order like their
+  // bits) picks the rank and its lane adds the replica's load.
+  if (warp == 0 && R <= 32) {
+    double my_load = 0.0;
+    int my_used = 0;
+    int e_n = oe[0], j_n = oj[0];
+    double q_n = per[e_n];
     for (int p = 0; p < P; ++p) {
-      int64_t bv = 0;
-      int bg = -1;
-      for (int r = lane; r < R; r += 32) {
-        const int64_t v = __double_as_longlong(load[r]);
-        if (used[r] < S && (bg < 0 || v < bv)) {
-          bv = v;
-          bg = r;
-        }
+      const int e = e_n, j = j_n;
+      const double q = q_n;
+      if (p + 1 < P) {  // the next replica's expert, index and load, read ahead
+        e_n = oe[p + 1];
+        j_n = oj[p + 1];
+        q_n = per[e_n];
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const int64_t ov = __shfl_down_sync(kFull, bv, o);
-        const int og = __shfl_down_sync(kFull, bg, o);
-        if (og >= 0 && (bg < 0 || ov < bv || (ov == bv && og < bg))) {
-          bv = ov;
-          bg = og;
-        }
-      }
-      if (lane == 0) {
-        const int e = oe[p], j = oj[p];
-        const int pid = bg * S + used[bg];
-        load[bg] += per[e];
-        used[bg] += 1;
+      const uint64_t key = lane < R && my_used < S ? (uint64_t)__double_as_longlong(my_load) : ~0ull;
+      const int g = warp_argmin64(key, lane);
+      if (g == lane) {
+        const int pid = g * S + my_used;
+        my_load += q;
+        my_used += 1;
         phys_to_logical[pid] = e;
-        phys_rank[pid] = bg;
+        phys_rank[pid] = g;
         logical_to_phys[stride * e + j] = pid;
+      }
+      __syncwarp();
+    }
+    if (lane < R) load[lane] = my_load;
+  } else if (warp == 0) {
+    // more ranks than lanes: lane l keeps the lightest of ranks l, l + 32, ... with a
+    // free slot, and only the winning rank's lane updates it and looks again
+    auto lane_best = [&](uint64_t *key, int *id) {
+      *key = ~0ull;
+      *id = -1;
+      for (int r = lane; r < R; r += 32) {
+        const uint64_t k = (uint64_t)__double_as_longlong(load[r]);
+        if (used[r] < S && (*id < 0 || k < *key)) {
+          *key = k;
+          *id = r;
+        }
+      }
+    };
+    uint64_t key;
+    int id;
+    lane_best(&key, &id);
+    int e_next = oe[0], j_next = oj[0];
+    for (int p = 0; p < P; ++p) {
+      const int e = e_next, j = j_next;
+      if (p + 1 < P) {
+        e_next = oe[p + 1];
+        j_next = oj[p + 1];
+      }
+      const int g = warp_argmin64(key, id < 0 ? 0x7fffffff : id);
+      if ((g & 31) == lane) {
+        const int pid = g * S + used[g];
+        load[g] += per[e];
+        used[g] += 1;
+        phys_to_logical[pid] = e;
+        phys_rank[pid] = g;
+        logical_to_phys[stride * e + j] = pid;
+        lane_best(&key, &id);
       }
       __syncwarp();
     }
