@@ -42,8 +42,11 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t f2bf(float f) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
 }
+// Two floats -> two bf16 (round to nearest even) in one conversion: lo in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return f2bf(lo) | (f2bf(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Two floats -> two OCP e4m3 codes (round to nearest even, saturate to +-448).
