@@ -84,7 +84,15 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 // silu for the e4m3 epilogue, whose result is rounded to e4m3 (3 mantissa bits):
-// the fast exponential and the approximate reciprocal (z -> -inf gives z * 0 = -0).
-__device__ __forceinline__ float silu_fast(float z) { return z * rcp_approx(1.0f + __expf(-z)); }
+// silu(z) = z * sigmoid(z) = z/2 + (z/2) * tanh(z/2), with the hardware tanh
+// approximation (tanh.approx.f32, relative error about 2^-11) -- one special-function
+// operation per value where exp + reciprocal take two.  Large |z| saturate tanh to
+// +-1 and give z or 0 exactly.
+__device__ __forceinline__ float silu_fast(float z) {
+  const float hz = 0.5f * z;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hz));
+  return fmaf(hz, t, hz);
+}
 
 }  // namespace moe
