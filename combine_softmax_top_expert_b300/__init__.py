@@ -20,8 +20,8 @@ __all__ = [
     "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
     "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
-    "moe_selftest_wait_timeout", "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_dispatch_layout_static",
+    "moe_last_cuda_error", "moe_selftest_wait_timeout", "EXPORTED",
     "MOE_DISPATCH_STATIC_SCRATCH_BYTES",
 ]
 
@@ -39,8 +39,8 @@ EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map"
             "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
     "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-            "moe_expert_gate_up", "moe_expert_down", "moe_dispatch_layout_static", "moe_last_cuda_error",
-            "moe_selftest_wait_timeout")
+            "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_dispatch_layout_static",
+            "moe_last_cuda_error", "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -119,6 +119,8 @@ def lib():
                                     c_vp, sz, c_vp, c_vp]),
             "moe_expert_gate_up": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp, c_i64, c_vp,
                                         c_vp, c_vp, c_vp]),
+            "moe_expert_gate_up_gather": (st, [c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp,
+                                               c_i64, c_vp, c_vp, c_vp]),
             "moe_expert_down": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_i64, c_vp, c_vp, c_vp]),
             "moe_combine": (st, [c_vp, c_i32, c_vp, c_vp, c_i64, c_i32, c_i64, c_vp, c_vp, c_i32, c_vp]),
             "moe_pack_weights": (st, [c_vp, c_vp, c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp,
@@ -256,6 +258,13 @@ def moe_expert_gate_up(x_perm, x_scales, phys_offsets, P, phys_to_logical, rows_
     _check("moe_expert_gate_up", lib().moe_expert_gate_up(
         _p(x_perm), _p(x_scales), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w),
         _p(shared_x), T_shared, _p(h), _p(h_scales), _p(err), _s(stream)))
+
+
+def moe_expert_gate_up_gather(x, T, row_to_token, phys_offsets, P, phys_to_logical, rows_hint, w, shared_x,
+                              T_shared, h, err=None, stream=None):
+    _check("moe_expert_gate_up_gather", lib().moe_expert_gate_up_gather(
+        _p(x), T, _p(row_to_token), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w),
+        _p(shared_x), T_shared, _p(h), _p(err), _s(stream)))
 
 
 def moe_expert_down(h, h_scales, phys_offsets, P, phys_to_logical, rows_hint, w, T_shared, y_perm, err=None,

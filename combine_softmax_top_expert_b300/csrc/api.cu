@@ -219,6 +219,28 @@ MOE_API moe_status_t moe_expert_gate_up(const void *x_perm, const float *x_scale
                  as_cuda(stream));
 }
 
+MOE_API moe_status_t moe_expert_gate_up_gather(const void *x, int64_t T, const int32_t *row_to_token,
+                                               const int32_t *phys_offsets, int64_t P,
+                                               const int32_t *phys_to_logical, int64_t rows_hint,
+                                               const moe_weights_t *w, const void *shared_x, int64_t T_shared,
+                                               void *h, int32_t *err, moe_stream_t stream) {
+  moe_status_t r = check_ffn(phys_offsets, P, rows_hint, w, T_shared);
+  if (r != MOE_OK) return r;
+  if (w->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (T < 0 || T > INT32_MAX || (T_shared > 0 && !shared_x) || !h) return MOE_ERR_INVALID_ARG;
+  if (rows_hint > 0 && (!x || T < 1 || !row_to_token)) return MOE_ERR_INVALID_ARG;
+  FfnArgs a = ffn_args(nullptr, nullptr, phys_offsets, P, phys_to_logical, rows_hint, w, shared_x, T_shared, h,
+                       nullptr, nullptr, err);
+  if (rows_hint > 0) {
+    a.gather_rows = row_to_token;
+    a.gather_x = x;
+    a.gather_T = T;
+  } else {
+    a.x_perm = nullptr;  // only the shared expert's rows: the plain kernel
+  }
+  return gate_up(a, as_cuda(stream));
+}
+
 MOE_API moe_status_t moe_expert_down(const void *h, const float *h_scales, const int32_t *phys_offsets, int64_t P,
                                      const int32_t *phys_to_logical, int64_t rows_hint, const moe_weights_t *w,
                                      int64_t T_shared, void *y_perm, int32_t *err, moe_stream_t stream) {

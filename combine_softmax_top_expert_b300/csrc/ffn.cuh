@@ -18,6 +18,11 @@ struct FfnArgs {
   float *h_scales;         // e4m3: [N + T_shared, I/128]
   void *y;                 // [N + T_shared, d]
   int32_t *err;
+  // bf16 gate/up only: when set, the routed rows are gathered from x [T, d] by
+  // row_to_token (gather_rows [N]) instead of read from x_perm
+  const int32_t *gather_rows = nullptr;
+  const void *gather_x = nullptr;
+  int64_t gather_T = 0;
 };
 
 // Largest p in [0, P) with offs[p] <= row (callers guarantee row < offs[P]).

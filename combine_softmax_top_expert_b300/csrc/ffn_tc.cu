@@ -53,10 +53,19 @@ struct Cfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-template <bool kGated, bool kSwap, int kBW>
+// kGather (gate/up, wide tiles only): the dispatch permute fused into the A-load.  The
+// routed token rows are gathered straight from x through row_to_token by the producer
+// warp: the 8 lanes of quarter g = lane / 8 copy the 8 16-byte chunks (c = lane % 8)
+// of tile rows 4i + g, i < 32, with cp.async, so each copy instruction reads 4 whole
+// 128-byte lines; chunk c of tile row r lands at chunk c ^ (r % 8) of its 128-byte
+// row, the layout a 128-row TMA box with 128-byte swizzle gives.  Each lane's copies
+// count as one arrival on the stage's barrier.  The weights still come by bulk copy;
+// the shared expert's rows are x itself and keep their tile load.
+template <bool kGated, bool kSwap, int kBW, bool kGather = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16(const Params p, const __grid_constant__ CUtensorMap tm_tok,
                       const __grid_constant__ CUtensorMap tm_sh) {
+  static_assert(!kGather || (kGated && !kSwap), "the gathered A-load is a wide gate/up tile");
   using C = Cfg<kGated, kSwap, kBW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -81,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), kGather ? 1 + 32 : 1);  // + one arrival per copying lane
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -113,26 +122,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(&misc[1]);
   const int total = tile_start[G];
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer
+  if (warp == 0 && (kGather || lane == 0)) {
+    // ------------------------------------------------ TMA producer (the whole warp with kGather)
     int s = 0, issued = 0;
     uint32_t ph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = grouped::decode<C::kTokTile>(p, tile_start, G, NT, tile);
       const CUtensorMap *tmt = (kGated && t.shared) ? &tm_sh : &tm_tok;
       const int nb = kSwap ? (t.valid + 15) / 16 : 0;
-      const uint32_t bytes = C::kABytes + (kSwap ? nb * 2048 : C::kBBytes);
+      const bool gathered = kGather && !t.shared;
+      // gathered rows past the group's end, or naming a token outside x (reported),
+      // are not loaded: they keep older data, and those outputs are never stored
+      const uint32_t bytes = (gathered ? 0 : C::kABytes) + (kSwap ? nb * 2048 : C::kBBytes);
+      const int g4 = lane >> 3, c8 = lane & 7;
+      int tok[kGather ? 32 : 1];
+#pragma unroll
+      for (int i = 0; i < (kGather ? 32 : 0); ++i) {
+        const int row = 4 * i + g4;
+        tok[i] = -1;
+        if (gathered && row < t.valid) {
+          const int v = p.gather_rows[t.tok_row + row];
+          if (v >= 0 && v < p.gather_T) tok[i] = v;
+          else raise_dev(p.err, MOE_DEV_LAYOUT);
+        }
+      }
       const int e = max(t.e, 0);
       // gated: the gate+up block of this tile's 128-feature block (swap tiles take
       // 64 of its features); down: the tile(s) of this block of output features
       const int rt0 = kGated ? (kSwap ? t.nt >> 1 : t.nt) : t.nt * (C::kFeatTile / 128);
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err)) {
+        bool waited = mbar_wait(empty(s), ph ^ 1, abort_flag, p.err);
+        // the gathering lanes give up together, so each stage they issue gets all its arrivals
+        if (kGather) waited = __all_sync(0xffffffffu, waited);
+        if (!waited) {
           ok = false;
           break;
         }
         const uint32_t st = stage0 + s * C::kStage, bar = full(s);
+        if (kGather) {
+          if (gathered) {
+            const uint8_t *col = p.gather_x + kb * 128 + c8 * 16;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int r = 4 * i + g4;
+              if (tok[i] >= 0) cp_async16(st + r * 128 + ((c8 ^ (r & 7)) << 4), col + (int64_t)tok[i] * p.gather_ld);
+            }
+          }
+          cp_async_arrive(bar);
+          if (lane != 0) {
+            ++issued;
+            if (++s == C::kStages) {
+              s = 0;
+              ph ^= 1;
+            }
+            continue;
+          }
+        }
         mbar_expect_tx(bar, bytes);
         const int kx = kb * 64;
         const uint32_t wdst = kSwap ? st : st + C::kABytes;
@@ -153,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kSwap) {
           for (int i = 0; i < nb; ++i) tma_load_2d(st + C::kABytes + i * 2048, tmt, bar, kx, t.tok_row + 16 * i);
-        } else {
+        } else if (!gathered) {
           tma_load_2d(st, tmt, bar, kx, t.tok_row);
         }
         ++issued;
@@ -164,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
+    if (kGather) cp_async_wait_all();  // this lane's row copies have landed
     if (*abort_flag) {  // let every copy still in flight land before the CTA exits
       for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
         mbar_wait_drain(full(j % C::kStages), (uint32_t)((j / C::kStages) & 1));
@@ -187,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         fence_after();
+        if (kGather) fence_proxy_async();  // rows written by cp.async, read by the MMA
         const uint32_t a = stage0 + s * C::kStage, bb = a + C::kABytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -294,10 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kGated, bool kSwap, int kBW>
+template <bool kGated, bool kSwap, int kBW, bool kGather = false>
 moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, cudaStream_t st) {
   using Cf = Cfg<kGated, kSwap, kBW>;
-  auto k = grouped_gemm_bf16<kGated, kSwap, kBW>;
+  auto k = grouped_gemm_bf16<kGated, kSwap, kBW, kGather>;
   if (cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem)) != MOE_OK)
     return MOE_ERR_CUDA;
   const int grid = grouped::sm_count();
@@ -321,13 +369,17 @@ moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I;
   if (f.N + f.T_shared == 0) return MOE_OK;
-  const grouped::Tiles kind = grouped::tile_kind(f.N + f.T_shared, f.P);
+  const bool gather = f.gather_rows != nullptr;
+  if (gather && (!f.gather_x || f.gather_T < 1 || f.gather_T > INT32_MAX || !aligned(f.gather_x, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const grouped::Tiles kind = gather ? grouped::Tiles::kWide : grouped::tile_kind(f.N + f.T_shared, f.P);
   if (kind == grouped::Tiles::kPair) return gate_up_bf16_pair(f, st);
   const bool swap = kind == grouped::Tiles::kSwap;
   const uint32_t tok_box = swap ? 16 : 128;
   CUtensorMap m_x, m_sh;
-  const void *xsrc = f.N > 0 ? f.x_perm : f.shared_x;
-  const int64_t xrows = f.N > 0 ? f.N : f.T_shared;
+  // gathered: the routed tiles read x by rows and need no map (one over x stands in)
+  const void *xsrc = gather ? f.gather_x : f.N > 0 ? f.x_perm : f.shared_x;
+  const int64_t xrows = gather ? f.gather_T : f.N > 0 ? f.N : f.T_shared;
   if (!grouped::make_map(&m_x, xsrc, xrows, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
   if (f.T_shared > 0) {
     if (!grouped::make_map(&m_sh, f.shared_x, f.T_shared, d, 2, tok_box)) return MOE_ERR_INVALID_ARG;
@@ -344,6 +396,13 @@ moe_status_t gate_up_bf16(const FfnArgs &f, cudaStream_t st) {
   p.shared_row0 = 0;
   p.out = f.h;
   p.ld = I;
+  if (gather) {
+    p.gather_rows = f.gather_rows;
+    p.gather_x = static_cast<const uint8_t *>(f.gather_x);
+    p.gather_ld = d * 2;
+    p.gather_T = (int)f.gather_T;
+    return launch<true, false, 128, true>(p, m_x, m_sh, st);
+  }
   return swap ? launch<true, true, 128>(p, m_x, m_sh, st) : launch<true, false, 128>(p, m_x, m_sh, st);
 }
 

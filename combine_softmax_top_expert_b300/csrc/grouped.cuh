@@ -40,6 +40,12 @@ struct Params {
   const float *a_scales;  // [rows, K/128] scales of the token operand
   const float *w_scales;  // [E_w, w_rows/128, K/128]
   float *out_scales;      // gate/up: [rows, I/128] scales of the quantised h
+  // gathered token operand (the dispatch permute fused into the bf16 gate/up A-load):
+  // routed row r is row gather_rows[r] of gather_x, gather_ld bytes apart
+  const int32_t *gather_rows;
+  const uint8_t *gather_x;
+  int64_t gather_ld;
+  int gather_T;  // rows of gather_x
 };
 
 struct Tile {

@@ -393,6 +393,27 @@ moe_status_t moe_expert_gate_up(const void *x_perm, const float *x_scales,
                                 int64_t T_shared, void *h, float *h_scales,
                                 int32_t *err, moe_stream_t stream);
 
+/* The dispatch copy fused into the first phase ("6.4 ...", section 3.1, steps 2
+ * and 3: each token's hidden state goes to the experts it picked, and each expert
+ * applies its gate and up matrices).  bf16 weights only.  Computes what
+ * moe_permute(x, MOE_BF16, T, d, k, slot_to_row, x_perm, MOE_BF16) followed by
+ * moe_expert_gate_up(x_perm, ...) computes, bit for bit, without writing x_perm:
+ * routed row r (phys_offsets order) reads row row_to_token[r] of x [T, d] bf16
+ * (16-byte aligned), row_to_token [rows_hint] int32 being the array
+ * moe_dispatch_layout writes.  The other arguments and h [N + T_shared, I] bf16 are
+ * those of moe_expert_gate_up.  Always runs the one-SM tiles of 128 token rows, and
+ * re-reads each gathered row once per 128 features of h, in 128-byte pieces: on
+ * prefill batches that costs more than the separate copy it saves, so the layer
+ * forward does not use it.  Returns MOE_ERR_UNSUPPORTED for other weight dtypes; a
+ * row_to_token entry outside [0, T) sets MOE_DEV_LAYOUT in *err and leaves that row
+ * of h unspecified. */
+moe_status_t moe_expert_gate_up_gather(const void *x, int64_t T, const int32_t *row_to_token,
+                                       const int32_t *phys_offsets, int64_t P,
+                                       const int32_t *phys_to_logical, int64_t rows_hint,
+                                       const moe_weights_t *w, const void *shared_x,
+                                       int64_t T_shared, void *h, int32_t *err,
+                                       moe_stream_t stream);
+
 /* The expert FFN's second phase on its own ("6.4 ...", section 2.1, the down
  * matrix): y = h W_down[e] for the rows moe_expert_gate_up wrote.  y_perm
  * [N + T_shared, d]: fp32 for f32 weights, else bf16. */

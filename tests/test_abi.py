@@ -148,6 +148,15 @@ def test_empty_batch_and_unsupported_shapes_without_gpu(lib):
     ws = moe.moe_ffn_workspace_size(64, 256, moe.MOE_E4M3)
     assert L.moe_expert_ffn(fake, fake, fake, 8, None, 64, ctypes.byref(w8), None, 0, fake, fake, ws, None,
                             None) == 2
+    # the gathered gate/up: bf16 weights only, a row map and a 16-byte aligned x
+    assert L.moe_expert_gate_up_gather(fake, 64, fake, fake, 8, None, 64, ctypes.byref(w8), None, 0, fake, None,
+                                       None) == 2
+    assert L.moe_expert_gate_up_gather(fake, 64, None, fake, 8, None, 64, ctypes.byref(w), None, 0, fake, None,
+                                       None) == 1
+    assert L.moe_expert_gate_up_gather(ctypes.c_void_p(264), 64, fake, fake, 8, None, 64, ctypes.byref(w), None,
+                                       0, fake, None, None) == 1
+    assert L.moe_expert_gate_up_gather(None, 0, None, fake, 8, None, 0, ctypes.byref(w), None, 0, fake, None,
+                                       None) == 0      # no rows: nothing queued
     # the shared expert needs its weight set
     assert L.moe_expert_ffn(fake, None, fake, 8, None, 64, ctypes.byref(w), fake, 16, fake, fake, 1 << 30, None,
                             None) == 1
