@@ -20,8 +20,8 @@ __all__ = [
     "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
     "moe_expert_ffn",
     "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-    "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_dispatch_layout_static",
-    "moe_last_cuda_error", "moe_selftest_wait_timeout", "EXPORTED",
+    "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_expert_down_combine",
+    "moe_dispatch_layout_static", "moe_last_cuda_error", "moe_selftest_wait_timeout", "EXPORTED",
     "MOE_DISPATCH_STATIC_SCRATCH_BYTES",
 ]
 
@@ -39,8 +39,8 @@ EXPORTED = ("moe_status_string", "moe_route", "moe_route_biased", "moe_eplb_map"
             "moe_dispatch_layout", "moe_permute", "moe_dequantize_e4m3", "moe_ffn_workspace_size",
     "moe_expert_ffn",
             "moe_combine", "moe_pack_weights", "moe_layer_workspace_size", "moe_layer_forward",
-            "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_dispatch_layout_static",
-            "moe_last_cuda_error", "moe_selftest_wait_timeout")
+            "moe_expert_gate_up", "moe_expert_gate_up_gather", "moe_expert_down", "moe_expert_down_combine",
+            "moe_dispatch_layout_static", "moe_last_cuda_error", "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -122,6 +122,8 @@ def lib():
             "moe_expert_gate_up_gather": (st, [c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_vp,
                                                c_i64, c_vp, c_vp, c_vp]),
             "moe_expert_down": (st, [c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_i64, c_vp, c_vp, c_vp]),
+            "moe_expert_down_combine": (st, [c_vp, c_vp, c_i64, c_vp, c_i64, _P(Weights), c_i64, c_vp, c_vp, c_vp,
+                                             c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
             "moe_combine": (st, [c_vp, c_i32, c_vp, c_vp, c_i64, c_i32, c_i64, c_vp, c_vp, c_i32, c_vp]),
             "moe_pack_weights": (st, [c_vp, c_vp, c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp,
                                       c_vp]),
@@ -272,6 +274,13 @@ def moe_expert_down(h, h_scales, phys_offsets, P, phys_to_logical, rows_hint, w,
     _check("moe_expert_down", lib().moe_expert_down(
         _p(h), _p(h_scales), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w), T_shared,
         _p(y_perm), _p(err), _s(stream)))
+
+
+def moe_expert_down_combine(h, phys_offsets, P, phys_to_logical, rows_hint, w, T_shared, row_to_token,
+                            slot_to_row, topk_w, T, k, y_perm, counts, out, err=None, stream=None):
+    _check("moe_expert_down_combine", lib().moe_expert_down_combine(
+        _p(h), _p(phys_offsets), P, _p(phys_to_logical), rows_hint, ctypes.byref(w), T_shared, _p(row_to_token),
+        _p(slot_to_row), _p(topk_w), T, k, _p(y_perm), _p(counts), _p(out), _p(err), _s(stream)))
 
 
 def moe_combine(y_perm, y_dt, slot_to_row, topk_w, T, k, d, shared_y, out, out_dt, stream=None):

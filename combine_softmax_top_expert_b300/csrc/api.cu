@@ -252,6 +252,31 @@ MOE_API moe_status_t moe_expert_down(const void *h, const float *h_scales, const
               as_cuda(stream));
 }
 
+MOE_API moe_status_t moe_expert_down_combine(const void *h, const int32_t *phys_offsets, int64_t P,
+                                             const int32_t *phys_to_logical, int64_t rows_hint,
+                                             const moe_weights_t *w, int64_t T_shared, const int32_t *row_to_token,
+                                             const int32_t *slot_to_row, const float *topk_w, int64_t T, int32_t k,
+                                             void *y_perm, int32_t *counts, void *out, int32_t *err,
+                                             moe_stream_t stream) {
+  moe_status_t r = check_ffn(phys_offsets, P, rows_hint, w, T_shared);
+  if (r != MOE_OK) return r;
+  if (w->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (T < 0 || k < 1 || k > 32 || rows_hint > T * (int64_t)k || (T_shared != 0 && T_shared != T))
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!h || !y_perm || !row_to_token || !slot_to_row || !topk_w || !counts || !out) return MOE_ERR_INVALID_ARG;
+  FfnArgs a = ffn_args(nullptr, nullptr, phys_offsets, P, phys_to_logical, rows_hint, w, nullptr, T_shared,
+                       const_cast<void *>(h), nullptr, y_perm, err);
+  a.c_row_to_token = row_to_token;
+  a.c_slot_to_row = slot_to_row;
+  a.c_topk_w = topk_w;
+  a.c_counts = counts;
+  a.c_out = out;
+  a.c_T = T;
+  a.c_k = k;
+  return down(a, as_cuda(stream));
+}
+
 MOE_API size_t moe_layer_workspace_size(const moe_shape_t *shape) {
   LayerPlan p;
   if (!plan_layer(shape, &p)) return 0;

@@ -35,6 +35,13 @@ __device__ __forceinline__ void raise_dev(int32_t *err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
+// A strong (relaxed, GPU-scope) load: reads what other threads' atomics left in L2.
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

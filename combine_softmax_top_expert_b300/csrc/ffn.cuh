@@ -23,6 +23,16 @@ struct FfnArgs {
   const int32_t *gather_rows = nullptr;
   const void *gather_x = nullptr;
   int64_t gather_T = 0;
+  // bf16 down only: when c_out is set, the combine runs in the down epilogue:
+  // c_out [c_T, d] = sum_j topk_w[t, j] y[slot_to_row[t, j]] (+ y[N + t]); c_counts
+  // [c_T, d / 128] is scratch
+  const int32_t *c_row_to_token = nullptr;
+  const int32_t *c_slot_to_row = nullptr;
+  const float *c_topk_w = nullptr;
+  int32_t *c_counts = nullptr;
+  void *c_out = nullptr;
+  int64_t c_T = 0;
+  int32_t c_k = 0;
 };
 
 // Largest p in [0, P) with offs[p] <= row (callers guarantee row < offs[P]).

@@ -53,6 +53,90 @@ struct Cfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
+// ---------------------------------------------------------------- fused combine
+// out[t] for one block of kFeat features, by one warp (lane: 8 features): the k rows
+// y[slot_to_row[t, j]] weighted in j order with fp32 fused multiply-adds, then the
+// shared expert's row y[N + t] added, then rounded to bf16 -- the same operations,
+// in the same order, as the separate combine kernel, so the result is identical.
+// The rows are read from L2 (other CTAs wrote them).
+template <int kFeat>
+__device__ __forceinline__ void combine_block(const Params &p, int tok, int nt, int lane) {
+  const uint16_t *y = static_cast<const uint16_t *>(p.out);
+  const int k = p.c_k;
+  const int64_t col = (int64_t)nt * kFeat;
+  const int32_t *s2r = p.c_slot_to_row + (int64_t)tok * k;
+  const float *tw = p.c_topk_w + (int64_t)tok * k;
+  for (int v = lane; v < kFeat / 8; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 raw[8];
+      int rr[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {  // all of the group's row loads go out first
+        int r = j0 + jj < k ? __ldg(s2r + j0 + jj) : -1;
+        if (r >= p.N) {
+          raise_dev(p.err, MOE_DEV_LAYOUT);
+          r = -1;
+        }
+        rr[jj] = r;
+        if (r >= 0) raw[jj] = __ldcg(reinterpret_cast<const uint4 *>(y + (int64_t)r * p.ld + col) + v);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (rr[jj] < 0) continue;
+        const float wt = __ldg(tw + j0 + jj);
+        const uint4 q = raw[jj];
+        const float f[8] = {bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y),
+                            bf16_lo(q.z), bf16_hi(q.z), bf16_lo(q.w), bf16_hi(q.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, f[i], acc[i]);
+      }
+    }
+    if (p.T_shared > 0) {
+      const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(y + (int64_t)(p.N + tok) * p.ld + col) + v);
+      const float f[8] = {bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y),
+                          bf16_lo(q.z), bf16_hi(q.z), bf16_lo(q.w), bf16_hi(q.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(1.0f, f[i], acc[i]);
+    }
+    reinterpret_cast<uint4 *>(p.c_out + (int64_t)tok * p.ld + col)[v] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// After a tile's rows of y are stored (every lane of an epilogue warp calls this for
+// its row r): count the row against its token's block, and let the warp sum the
+// blocks whose last row this was.  Counting is release (fence, then the atomic);
+// summing is acquire (a strong read of the count, then a fence).  No CTA waits for
+// another: whichever CTA completes a block does its sum.
+template <int kFeat>
+__device__ __forceinline__ void combine_after_rows(const Params &p, const Tile &t, int r, int lane, int NT) {
+  int tok = -1;
+  bool last = false;
+  if (t.e >= 0 && r < t.valid) {
+    const int row = t.out_row + r;
+    tok = t.shared ? row - p.N : __ldg(p.c_row_to_token + row);
+    if (tok >= 0 && tok < p.c_T) {
+      __threadfence();
+      last = atomicAdd(p.c_counts + (int64_t)tok * NT + t.nt, 1) == -1;
+    } else {
+      raise_dev(p.err, MOE_DEV_LAYOUT);
+    }
+  }
+  unsigned m = __ballot_sync(0xffffffffu, last);
+  while (m) {
+    const int src = __ffs(m) - 1;
+    m &= m - 1;
+    const int tk = __shfl_sync(0xffffffffu, tok, src);
+    (void)ld_relaxed_gpu(p.c_counts + (int64_t)tk * NT + t.nt);
+    __threadfence();
+    combine_block<kFeat>(p, tk, t.nt, lane);
+  }
+}
+
 // kGather (gate/up, wide tiles only): the dispatch permute fused into the A-load.  The
 // routed token rows are gathered straight from x through row_to_token by the producer
 // warp: the 8 lanes of quarter g = lane / 8 copy the 8 16-byte chunks (c = lane % 8)
@@ -61,11 +145,15 @@ struct Cfg {
 // row, the layout a 128-row TMA box with 128-byte swizzle gives.  Each lane's copies
 // count as one arrival on the stage's barrier.  The weights still come by bulk copy;
 // the shared expert's rows are x itself and keep their tile load.
-template <bool kGated, bool kSwap, int kBW, bool kGather = false>
+// kCombine (down, wide tiles only): the combine fused into the epilogue
+// (combine_after_rows); the shared expert's group is tiled first, so that the blocks'
+// last rows, and with them the sums, spread over the routed tiles.
+template <bool kGated, bool kSwap, int kBW, bool kGather = false, bool kCombine = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16(const Params p, const __grid_constant__ CUtensorMap tm_tok,
                       const __grid_constant__ CUtensorMap tm_sh) {
   static_assert(!kGather || (kGated && !kSwap), "the gathered A-load is a wide gate/up tile");
+  static_assert(!kCombine || (!kGated && !kSwap), "the fused combine is a wide down tile");
   using C = Cfg<kGated, kSwap, kBW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,7 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const Tile t = grouped::decode<C::kTokTile>(p, tile_start, G, NT, tile);
       const int b = it & 1;
-      if (!mbar_wait(tfull(b), (it >> 1) & 1, abort_flag, p.err)) break;
+      bool waited = mbar_wait(tfull(b), (it >> 1) & 1, abort_flag, p.err);
+      if (kCombine) waited = __all_sync(0xffffffffu, waited);  // the warp's lanes stay together
+      if (!waited) break;
       fence_after();
       if (t.e < 0 && r == 0) raise_dev(p.err, MOE_DEV_LAYOUT);
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * C::kAccCols;
@@ -331,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_before();
       mbar_arrive_relaxed(tempty(b));
+      if (kCombine) combine_after_rows<C::kFeatTile>(p, t, r, lane, NT);
     }
   }
   fence_before();
@@ -342,10 +433,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kGated, bool kSwap, int kBW, bool kGather = false>
+// The fused combine's counts: each (token, feature block) starts at minus the rows
+// the token has (its slots with a row, plus its shared row).  A token with none gets
+// out = 0 here, as the separate combine gives it.
+__global__ void combine_counts_init(const int32_t *__restrict__ s2r, int T, int k, int N, int with_shared, int NT,
+                                    int32_t *__restrict__ counts, uint16_t *__restrict__ out, int64_t d) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    int need = with_shared;
+    for (int j = 0; j < k; ++j) {
+      const int r = s2r[(int64_t)t * k + j];
+      need += (r >= 0 && r < N) ? 1 : 0;
+    }
+    for (int nt = 0; nt < NT; ++nt) counts[(int64_t)t * NT + nt] = -need;
+    if (need == 0)
+      for (int64_t c = 0; c < d; c += 8) *reinterpret_cast<uint4 *>(out + (int64_t)t * d + c) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <bool kGated, bool kSwap, int kBW, bool kGather = false, bool kCombine = false>
 moe_status_t launch(const Params &p, const CUtensorMap &a, const CUtensorMap &b, cudaStream_t st) {
   using Cf = Cfg<kGated, kSwap, kBW>;
-  auto k = grouped_gemm_bf16<kGated, kSwap, kBW, kGather>;
+  auto k = grouped_gemm_bf16<kGated, kSwap, kBW, kGather, kCombine>;
   if (cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem)) != MOE_OK)
     return MOE_ERR_CUDA;
   const int grid = grouped::sm_count();
@@ -412,7 +520,12 @@ moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
   const moe_weights_t &w = *f.w;
   const int64_t d = w.d, I = w.I, rows = f.N + f.T_shared;
   if (rows == 0) return MOE_OK;
-  const grouped::Tiles kind = grouped::tile_kind(rows, f.P);
+  const bool fused = f.c_out != nullptr;
+  if (fused && (!f.c_row_to_token || !f.c_slot_to_row || !f.c_topk_w || !f.c_counts || f.c_T < 1 ||
+                f.c_T > INT32_MAX / 32 || f.c_k < 1 || f.c_k > 32 || (f.T_shared != 0 && f.T_shared != f.c_T) ||
+                !aligned(f.c_out, 16) || !aligned(f.y, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const grouped::Tiles kind = fused ? grouped::Tiles::kWide : grouped::tile_kind(rows, f.P);
   const int kbw = (d % 256 == 0) ? 256 : 128;
   if (kind == grouped::Tiles::kPair && kbw == 256) return down_bf16_pair(f, st);
   const bool swap = kind == grouped::Tiles::kSwap;
@@ -428,6 +541,23 @@ moe_status_t down_bf16(const FfnArgs &f, cudaStream_t st) {
   p.shared_row0 = (int)f.N;
   p.out = f.y;
   p.ld = d;
+  if (fused) {
+    p.c_row_to_token = f.c_row_to_token;
+    p.c_slot_to_row = f.c_slot_to_row;
+    p.c_topk_w = f.c_topk_w;
+    p.c_counts = f.c_counts;
+    p.c_out = static_cast<uint16_t *>(f.c_out);
+    p.c_k = f.c_k;
+    p.c_T = (int)f.c_T;
+    p.shared_first = 1;
+    const int NTc = (int)(d / kbw);
+    const int blocks = (int)((f.c_T + 255) / 256);
+    combine_counts_init<<<blocks < 1184 ? blocks : 1184, 256, 0, st>>>(
+        f.c_slot_to_row, (int)f.c_T, f.c_k, (int)f.N, f.T_shared > 0 ? 1 : 0, NTc, f.c_counts, p.c_out, d);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    return kbw == 256 ? launch<false, false, 256, false, true>(p, m_h, m_h, st)
+                      : launch<false, false, 128, false, true>(p, m_h, m_h, st);
+  }
   if (swap) return launch<false, true, 128>(p, m_h, m_h, st);
   return kbw == 256 ? launch<false, false, 256>(p, m_h, m_h, st) : launch<false, false, 128>(p, m_h, m_h, st);
 }

@@ -46,7 +46,25 @@ struct Params {
   const uint8_t *gather_x;
   int64_t gather_ld;
   int gather_T;  // rows of gather_x
+  // the combine fused into the bf16 down epilogue: out[t] = sum_j topk_w[t, j] *
+  // y[slot_to_row[t, j]] (+ y[N + t]) for the c_T tokens, each 128/256-feature block
+  // summed by the tile that writes its last row (c_counts [c_T, feat / tile
+  // features] starts at minus the rows each token has)
+  const int32_t *c_row_to_token;
+  const int32_t *c_slot_to_row;
+  const float *c_topk_w;
+  int32_t *c_counts;
+  uint16_t *c_out;
+  int c_k, c_T;
+  int shared_first;  // 1: the shared expert's group is tiled first
 };
+
+// Group at position g of the tile order: the routed groups 0..P-1, then the shared
+// expert's (P), or with shared_first the shared expert's first.
+__device__ __forceinline__ int group_at(const Params &p, int g) {
+  if (!p.shared_first || p.T_shared == 0) return g;
+  return g == 0 ? p.P : g - 1;
+}
 
 struct Tile {
   int e, tok_row, out_row, valid, nt;
@@ -110,7 +128,7 @@ template <int kTokTile>
 __device__ __forceinline__ void build_tile_table(const Params &p, int *tile_start, int G, int NT) {
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     int r0, n;
-    group_span(p, g, &r0, &n);
+    group_span(p, group_at(p, g), &r0, &n);
     tile_start[g + 1] = n > 0 ? ((n + kTokTile - 1) / kTokTile) * NT : 0;
   }
   if (threadIdx.x == 0) tile_start[0] = 0;
@@ -128,7 +146,7 @@ __device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, i
     if (tile_start[mid] <= tile) lo = mid;
     else hi = mid - 1;
   }
-  const int g = lo, local = tile - tile_start[g];
+  const int g = group_at(p, lo), local = tile - tile_start[lo];
   int r0, n;
   group_span(p, g, &r0, &n);
   const int MT = (n + kTokTile - 1) / kTokTile;

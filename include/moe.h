@@ -423,6 +423,29 @@ moe_status_t moe_expert_down(const void *h, const float *h_scales,
                              const moe_weights_t *w, int64_t T_shared, void *y_perm,
                              int32_t *err, moe_stream_t stream);
 
+/* The combine fused into the down phase ("6.4 ...", section 3.1, steps 3 and 4:
+ * each expert applies its down matrix, then each token's k expert outputs are
+ * summed with its route weights).  bf16 weights only.  Writes y_perm as
+ * moe_expert_down does (bf16 [rows_hint + T_shared, d]) and out [T, d] bf16
+ * identical to moe_combine(y_perm, MOE_BF16, slot_to_row, topk_w, T, k, d,
+ * T_shared ? y_perm + rows_hint * d : NULL, out, MOE_BF16): every block of 128 or
+ * 256 features of out[t] is summed, in j order with fp32 fused multiply-adds, by
+ * whichever tile writes the last of the token's rows for that block.
+ * row_to_token [rows_hint] and slot_to_row [T, k] are the arrays moe_dispatch_layout
+ * writes; topk_w [T, k] fp32; T_shared is 0 or T (the shared expert's rows, from
+ * moe_expert_gate_up, follow the routed ones in h); counts is caller scratch of
+ * T * (d / 128) int32, overwritten.  k <= 32; always runs the one-SM tiles of 128
+ * token rows; y_perm and out 16-byte aligned.  Returns MOE_ERR_UNSUPPORTED for
+ * other weight dtypes.  A row whose token is outside [0, T) sets MOE_DEV_LAYOUT and
+ * leaves that token's out unspecified. */
+moe_status_t moe_expert_down_combine(const void *h, const int32_t *phys_offsets, int64_t P,
+                                     const int32_t *phys_to_logical, int64_t rows_hint,
+                                     const moe_weights_t *w, int64_t T_shared,
+                                     const int32_t *row_to_token, const int32_t *slot_to_row,
+                                     const float *topk_w, int64_t T, int32_t k, void *y_perm,
+                                     int32_t *counts, void *out, int32_t *err,
+                                     moe_stream_t stream);
+
 /* Combine ("6.4 ...", section 3.1, step 4: weighted-sum by route weights).
  * out[t] = sum_{j<k} topk_w[t, j] * y_perm[slot_to_row[t, j]] (+ shared_y[t]),
  * fp32 accumulation in j order, then rounded to out_dt.  y_perm [N, d] and shared_y

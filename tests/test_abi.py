@@ -157,6 +157,14 @@ def test_empty_batch_and_unsupported_shapes_without_gpu(lib):
                                        0, fake, None, None) == 1
     assert L.moe_expert_gate_up_gather(None, 0, None, fake, 8, None, 0, ctypes.byref(w), None, 0, fake, None,
                                        None) == 0      # no rows: nothing queued
+    # the down phase with the combine fused: bf16 weights only, T_shared 0 or T, k <= 32
+    dc = lambda ww, T_sh, T, k, N=64: L.moe_expert_down_combine(fake, fake, 8, None, N, ctypes.byref(ww), T_sh, fake,
+                                                                fake, fake, T, k, fake, fake, fake, None, None)
+    assert dc(w8, 0, 32, 2) == 2
+    assert dc(w, 5, 32, 2) == 1          # a shared expert over part of the batch
+    assert dc(w, 0, 32, 33) == 1         # k above 32
+    assert dc(w, 0, 16, 2) == 1          # more rows than T * k
+    assert dc(w, 0, 0, 2, N=0) == 0      # empty batch: nothing queued
     # the shared expert needs its weight set
     assert L.moe_expert_ffn(fake, None, fake, 8, None, 64, ctypes.byref(w), fake, 16, fake, fake, 1 << 30, None,
                             None) == 1
