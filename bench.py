@@ -56,6 +56,11 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=256, help="tokens in the CPU-baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=2, help="tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compare-fused", action="store_true",
+                    help="bf16 workloads: time the two fused expert-FFN entry points against the separate steps "
+                         "(one JSON line of per-call times; not the contract line)")
+    ap.add_argument("--fused-only", choices=["gather", "combine"],
+                    help="with --compare-fused: run only that fused call (and what it reads), e.g. under a profiler")
     ap.add_argument("--override", action="append", default=[], metavar="FIELD=INT",
                     help="change an integer field of the workload (T, E, R, k, d, I, n_redundant, eplb_placement, "
                          "expert_placement, fp8_dispatch), e.g. for a small profiling case")
@@ -644,8 +649,127 @@ def run_reference(args, world, rank):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_compare_fused(args):
+    """Per-call device times (median of --steps calls, each after an L2 flush, after
+    --warmup calls) of the permute fused into the gate/up GEMM and of the combine fused
+    into the down GEMM, beside the separate calls they replace, on one bf16 workload;
+    and whether each fused result equals the separate calls' bit for bit."""
+    import torch
+
+    import combine_softmax_top_expert_b300 as moe
+    from combine_softmax_top_expert_b300.layer import PackedWeights
+
+    cfg = workload(args)
+    if cfg.dtype != "bf16" or cfg.n_redundant or cfg.expert_placement or cfg.fp8_dispatch:
+        return {"mode": "compare_fused", "workload": cfg.name,
+                "unavailable": "the fused entry points take bf16 experts; pick a bf16 workload without EPLB"}
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, E, k, R, d, I, N = cfg.T, cfg.E, cfg.k, cfg.R, cfg.d, cfg.I, cfg.N
+    T_sh = T if cfg.shared else 0
+    pw = PackedWeights(E, d, I, moe.MOE_BF16, cfg.shared, device=dev)
+    for e in range(E):
+        pw.pack(e, *(mi.make_weight_device(cfg, w, e, dev) for w in ("w_gate", "w_up", "w_down")))
+    if cfg.shared:
+        pw.pack(E, *(mi.make_weight_device(cfg, w, 0, dev) for w in ("ws_gate", "ws_up", "ws_down")))
+    W = pw.struct()
+    logits = torch.from_numpy(mi.make_logits(cfg)).to(dev)
+    x = torch.from_numpy(mi.make_x(cfg).view(np.int16)).to(dev).view(torch.bfloat16)
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids, tw = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    lc, pc, po = torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    rc, ro, r2t, s2r = torch.empty(R, **i32), torch.empty(R + 1, **i32), torch.empty(N, **i32), torch.empty((T, k), **i32)
+    stats, err = torch.empty(16, **i32), torch.zeros(1, **i32)
+    dws_b = moe.moe_dispatch_workspace_size(T, k, E)
+    dws = torch.empty(dws_b, dtype=torch.uint8, device=dev)
+    moe.moe_route(logits, T, E, k, ids, tw, err)
+    moe.moe_dispatch_layout(ids, T, k, E, R, None, lc, pc, po, rc, ro, r2t, s2r, stats, dws, dws_b, err)
+    rows = N + T_sh
+    sx = x if T_sh else None
+    xp = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    h, h2 = (torch.empty((rows, I), dtype=torch.bfloat16, device=dev) for _ in range(2))
+    y, y2 = (torch.empty((rows, d), dtype=torch.bfloat16, device=dev) for _ in range(2))
+    out, out2 = (torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(2))
+    counts = torch.empty(T * (d // 128), **i32)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def tiles(mode, fn):
+        def run():
+            os.environ["MOE_B300_FFN_TILES"] = mode
+            try:
+                fn()
+            finally:
+                del os.environ["MOE_B300_FFN_TILES"]
+        return run if mode else fn
+
+    permute = lambda: moe.moe_permute(x, moe.MOE_BF16, T, d, k, s2r, xp, moe.MOE_BF16)
+    gate_up = lambda: moe.moe_expert_gate_up(xp, None, po, E, None, N, W, sx, T_sh, h, None, err)
+    gathered = lambda: moe.moe_expert_gate_up_gather(x, T, r2t, po, E, None, N, W, sx, T_sh, h2, err)
+    down = lambda: moe.moe_expert_down(h, None, po, E, None, N, W, T_sh, y, err)
+    combine = lambda: moe.moe_combine(y, moe.MOE_BF16, s2r, tw, T, k, d, y[N:] if T_sh else None, out, moe.MOE_BF16)
+    fused = lambda: moe.moe_expert_down_combine(h, po, E, None, N, W, T_sh, r2t, s2r, tw, T, k, y2, counts, out2, err)
+    if args.fused_only:
+        # only the fused call, its inputs made once by other kernels (the pair-tile
+        # gate/up for h), so that a profiler's name filter sees just the fused launches
+        fn = gathered if args.fused_only == "gather" else fused
+        if args.fused_only == "combine":
+            tiles("pair", gate_up)()
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        return {"mode": "compare_fused", "workload": cfg.name, "fused_only": args.fused_only,
+                "calls": args.warmup + args.steps, "err": int(err.item())}
+    calls = {
+        "permute": permute,
+        "gate_up (default tiles)": gate_up,
+        "gate_up (wide tiles)": tiles("wide", gate_up),
+        "permute + gate_up (default tiles)": lambda: (permute(), gate_up()),
+        "permute + gate_up (wide tiles)": tiles("wide", lambda: (permute(), gate_up())),
+        "gate_up with the permute fused": gathered,
+        "down (default tiles)": down,
+        "down (wide tiles)": tiles("wide", down),
+        "combine": combine,
+        "down + combine (default tiles)": lambda: (down(), combine()),
+        "down + combine (wide tiles)": tiles("wide", lambda: (down(), combine())),
+        "down with the combine fused": fused,
+    }
+    us = {}
+    props = torch.cuda.get_device_properties(dev)
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else None
+    with ClockSampler(uuid) as clk:
+        for name, fn in calls.items():
+            for _ in range(args.warmup):
+                fn()
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            us[name] = round(float(np.median(ts)), 1)
+    # bit-identity on the wide tiles the fused kernels use
+    tiles("wide", lambda: (permute(), gate_up()))()
+    gathered()
+    tiles("wide", lambda: (down(), combine()))()
+    fused()
+    torch.cuda.synchronize()
+    same = {"gate_up with the permute fused": bool(torch.equal(h.view(torch.int16), h2.view(torch.int16))),
+            "down with the combine fused: y_perm": bool(torch.equal(y.view(torch.int16), y2.view(torch.int16))),
+            "down with the combine fused: out": bool(torch.equal(out.view(torch.int16), out2.view(torch.int16)))}
+    return {"mode": "compare_fused", "workload": cfg.name, "config": workload_config(cfg), "unit": "us per call",
+            "steps": args.steps, "warmup": args.warmup, "l2": "flushed before each call (512 MiB write)",
+            "us": us, "bit_identical": same, "err": int(err.item()), "clocks": clk.summary()}
+
+
 def main():
     args = parse()
+    if args.compare_fused:
+        line = run_compare_fused(args)
+        print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":     # rank 0 alone times the oracle; no process group
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         line = run_reference(args, world, rank)
