@@ -54,6 +54,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try, but a thread whose phase is not complete sleeps until it completes
 // or `hint_ns` has passed, instead of returning at once: waiting warps then leave
 // the issue slots to the warps doing work.
@@ -76,6 +89,7 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, ui
 // clock between sleeps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
                                           uint64_t timeout_ns = kTimeoutNs) {
+  if (mbar_test(bar, parity)) return true;  // already complete: no suspend
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
     if (mbar_try(bar, parity)) return true;
