@@ -80,6 +80,22 @@ __device__ __forceinline__ void fma2_scaled(float *acc, const float *v, float f)
         : "f"(v[i]), "f"(v[i + 1]), "f"(f));
 }
 
+// acc[i] = fma(acc[i], f, +0) for even n, two lanes per instruction: the first fold
+// of a block sequence with the block already in acc, rounded as fma2_scaled into zeros.
+template <int n>
+__device__ __forceinline__ void scale2_inplace(float *acc, float f) {
+#pragma unroll
+  for (int i = 0; i < n; i += 2)
+    asm("{\n\t.reg .b64 a, s, z;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 s, {%2, %2};\n\t"
+        "mov.b64 z, 0;\n\t"
+        "fma.rn.f32x2 a, a, s, z;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(acc[i]), "+f"(acc[i + 1])
+        : "f"(f));
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Reciprocal by the hardware approximation (rcp.approx.ftz.f32: about 1 ulp;

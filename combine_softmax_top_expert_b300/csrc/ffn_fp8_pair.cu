@@ -232,6 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.s1 = kGated ? __ldg(p.w_scales + c.sw1) : 0.f;
       return c;
     };
+    // down: the second half of a finished tile's outputs (this thread's columns
+    // c1..c1+63 of its row, packed to bf16) waits in pk until the next tile's first
+    // accumulator is read and released, so the MMA runs on while it is stored
+    uint32_t pk[32];
+    bool pend = false, pend_ok = false;
+    int pend_x = 0, pend_grow = 0;
+    uint8_t *pend_dst = nullptr;
+    auto store_pend = [&]() {
+      if (pend) {
+        store_rows(pk, pend_x, pend_ok, pend_grow, pend_dst);
+        store_rows(pk + 16, pend_x + 32, pend_ok, pend_grow, pend_dst + 64);
+        pend = false;
+      }
+    };
     int gk = 0, it = 0;
     TileCtx cur;
     if (!kGated && pair < total) cur = prep(pair);
@@ -241,12 +255,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = cur.row_ok;
       const int grow = cur.grow, sw0 = cur.sw0, sw1 = cur.sw1, sa = cur.sa;
       float acc0[64], acc1[64];  // gated: gate, up of 64 features; down: columns c0.., c1..
+      if (kGated) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
+        for (int i = 0; i < 64; ++i) acc0[i] = acc1[i] = 0.f;
+      }
       bool ok = true;
       // the scales of the next K block load one block ahead
       float xs_n = cur.xs, s0_n = cur.s0, s1_n = cur.s1;
-      for (int kb = 0; kb < KB; ++kb, ++gk) {
+      int kb0 = 0;
+      if (!kGated) {
+        // block 0 goes straight into the sums; once its accumulator is released, the
+        // previous tile's deferred half is stored
+        const int b = gk & 1;
+        const float f0 = xs_n * s0_n;
+        if (KB > 1) {
+          xs_n = row_ok ? __ldg(p.a_scales + sa + 1) : 0.f;
+          s0_n = __ldg(p.w_scales + sw0 + 1);
+        }
+        if (!mbar_wait(dfull(b), (gk >> 1) & 1, abort_flag, p.err)) break;
+        fence_after();
+        const uint32_t d = lane_base + b * kAccCols;
+        tmem_ld32(d + c0, acc0);
+        tmem_ld32(d + c0 + 32, acc0 + 32);
+        tmem_ld32(d + c1, acc1);
+        tmem_ld32(d + c1 + 32, acc1 + 32);
+        tmem_wait_ld();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive_relaxed(dempty(b));
+          else mbar_arrive_cluster_relaxed(peer_addr(dempty(b), 0));
+        }
+        store_pend();
+        scale2_inplace<64>(acc0, f0);
+        scale2_inplace<64>(acc1, f0);
+        ++gk;
+        kb0 = 1;
+      }
+      for (int kb = kb0; kb < KB; ++kb, ++gk) {
         const int b = gk & 1;
         const float f0 = xs_n * s0_n;
         const float f1 = kGated ? xs_n * s1_n : f0;
@@ -308,16 +354,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                             t.nt * 128 + 64 * half);
         if (row_ok && half == 0) p.out_scales[(int64_t)grow * (p.feat / 128) + t.nt] = scale;
       } else {
-        // four 32-column pieces of this thread's 128 output features
+        // four 32-column pieces of this thread's 128 output features: the first two now,
+        // the last two after the next tile's first block (at once on the last tile)
+        uint8_t *dst = static_cast<uint8_t *>(p.out) + ((int64_t)grow * p.ld + t.nt * 256 + 128 * half) * 2;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float *a = c < 2 ? acc0 + 32 * c : acc1 + 32 * (c - 2);
+        for (int c = 0; c < 2; ++c) {
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
-          store_rows(w, t.nt * 256 + 128 * half + 32 * c, row_ok, grow,
-                     static_cast<uint8_t *>(p.out) + ((int64_t)grow * p.ld + t.nt * 256 + 128 * half + 32 * c) * 2);
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(acc0[32 * c + 2 * i], acc0[32 * c + 2 * i + 1]);
+          store_rows(w, t.nt * 256 + 128 * half + 32 * c, row_ok, grow, dst + 64 * c);
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(acc1[2 * i], acc1[2 * i + 1]);
+        pend = true;
+        pend_ok = row_ok;
+        pend_grow = grow;
+        pend_x = t.nt * 256 + 128 * half + 64;
+        pend_dst = dst + 128;
+        if (tile + npairs >= total) store_pend();  // this CTA's last tile
       }
     }
     if (lane == 0) bulk_wait();
