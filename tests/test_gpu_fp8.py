@@ -97,3 +97,16 @@ def test_ffn_fp8_skewed_groups_and_ragged_tiles(mode):
 def test_ffn_fp8_single_token(mode):
     run_ffn_fp8(SMALL.scaled(T=1), mode=mode)
 
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_ffn_fp8_one_k_block(mode):
+    # I = 128: the down projection's only K block is also its first one
+    run_ffn_fp8(SMALL.scaled(I=128), mode=mode)
+
+
+def test_ffn_fp8_more_tiles_than_sm_pairs():
+    # at least 128 down tiles of 256 x 256 for the GPU's SM pairs: each pair runs
+    # several tiles, so part of a tile's outputs leaves after the next tile's first block
+    cfg = SMALL.scaled(T=2048, d=1024, E=8, k=4, I=256)
+    run_ffn_fp8(cfg, mode="pair")
