@@ -158,8 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < total && ok; tile += npairs) {
         for (int kb = 0; kb < KB; ++kb, ++gk) {
           const int b = gk & 1;
-          if (!mbar_wait(full(s), ph, abort_flag, p.err) ||
-              !mbar_wait(dempty(b), ((gk >> 1) & 1) ^ 1, abort_flag, p.err)) {
+          if (!mbar_wait2(full(s), ph, dempty(b), ((gk >> 1) & 1) ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
