@@ -118,3 +118,10 @@ def test_ffn_pair_tile_edges():
     lay = run_ffn(cfg, "pair", logits=l)
     counts = np.diff(lay["phys_offsets"])
     assert counts.max() > 512 and (counts == 0).any()
+
+
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
+def test_ffn_smallest_dims(mode):
+    # d = I = 128: one K block and one feature tile in every GEMM (d < 256, so the pair
+    # orientation's down projection runs on one-SM tiles)
+    run_ffn(SMALL.scaled(T=50, d=128, I=128, E=4, k=2, R=2, shared=True), mode)
