@@ -215,9 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int grow, sw0, sw1, sa;
       float xs, s0, s1;
     };
+    grouped::GroupCache gcache;
     auto prep = [&](int tile) {
       TileCtx c;
-      c.t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile);
+      c.t = grouped::decode<kTokTile>(p, tile_start, G, NT, tile, &gcache);
       const int row = 128 * (int)rank + r;
       c.row_ok = row < c.t.valid && c.t.e >= 0;
       c.grow = c.t.out_row + (c.row_ok ? row : 0);  // also the row of the token operand's scales

@@ -136,19 +136,36 @@ __device__ __forceinline__ void build_tile_table(const Params &p, int *tile_star
   block_scan(tile_start + 1, G);
 }
 
+// The group a thread decoded last: its tile range and what decode reads from global
+// memory for it, so the next tile of the same group is decoded from registers.
+struct GroupCache {
+  int lo = 0, hi = 0;  // tiles [lo, hi); empty until the first decode
+  int g, r0, n, e;
+};
+
 // kTokTile == 32 (swap): token tiles of one feature block run back to back.
 // Otherwise (wide): feature blocks of one token tile run back to back.
 template <int kTokTile>
-__device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, int G, int NT, int tile) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tile_start[mid] <= tile) lo = mid;
-    else hi = mid - 1;
+__device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, int G, int NT, int tile,
+                                       GroupCache *cache = nullptr) {
+  int g, r0, n, e, local;
+  if (cache && tile >= cache->lo && tile < cache->hi) {
+    g = cache->g, r0 = cache->r0, n = cache->n, e = cache->e;
+    local = tile - cache->lo;
+  } else {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    g = group_at(p, lo);
+    local = tile - tile_start[lo];
+    group_span(p, g, &r0, &n);
+    e = g >= p.P ? p.E_w - 1 : (p.p2l ? p.p2l[g] : g);
+    if (e < 0 || e >= p.E_w) e = -1;
+    if (cache) *cache = GroupCache{tile_start[lo], tile_start[lo + 1], g, r0, n, e};
   }
-  const int g = group_at(p, lo), local = tile - tile_start[lo];
-  int r0, n;
-  group_span(p, g, &r0, &n);
   const int MT = (n + kTokTile - 1) / kTokTile;
   int mt, nt;
   if (kTokTile == 32) {
@@ -160,8 +177,6 @@ __device__ __forceinline__ Tile decode(const Params &p, const int *tile_start, i
   }
   Tile t;
   t.shared = g >= p.P;
-  int e = t.shared ? p.E_w - 1 : (p.p2l ? p.p2l[g] : g);
-  if (e < 0 || e >= p.E_w) e = -1;
   t.e = e;
   t.nt = nt;
   t.valid = min(kTokTile, n - mt * kTokTile);
