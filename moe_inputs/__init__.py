@@ -171,6 +171,9 @@ CONFIGS = [
 ]
 
 
+NAMES = tuple(c.name for c in CONFIGS)
+
+
 def config(name_or_index) -> LayerConfig:
     if isinstance(name_or_index, int):
         return CONFIGS[name_or_index]

@@ -65,16 +65,18 @@ def guarded_layer(cfg):
 
 
 CASES = [
-    ("fp32, ragged", mi.config(0).scaled(T=37)),
+    ("fp32, ragged", mi.config("tiny_fp32").scaled(T=37)),
     ("bf16 + shared, pair gate/up and wide down (d = 384)",
-     mi.config(2).scaled(T=300, d=384, E=16, k=4, I=256, R=4)),
-    ("bf16 decode-shaped: swap tiles", mi.config(1).scaled(T=16, d=256, E=64, k=8, I=256, R=8)),
+     mi.config("prefill_bf16_skew").scaled(T=300, d=384, E=16, k=4, I=256, R=4)),
+    ("bf16 decode-shaped: swap tiles", mi.config("decode_bf16").scaled(T=16, d=256, E=64, k=8, I=256, R=8)),
     ("bf16 + shared, load-aware EPLB, FP8 dispatch",
-     mi.config(3).scaled(T=512, d=512, E=32, k=8, I=256, R=8, n_redundant=8, eplb_placement=1, fp8_dispatch=1)),
+     mi.config("prefill_bf16_skew_eplb").scaled(T=512, d=512, E=32, k=8, I=256, R=8, n_redundant=8, eplb_placement=1,
+                                                fp8_dispatch=1)),
     ("bf16, EPLB hottest replicas, round-robin placement",
-     mi.config(3).scaled(T=260, d=256, E=16, k=4, I=256, R=4, n_redundant=4, expert_placement=1)),
-    ("e4m3 experts, pair tiles", mi.config(4).scaled(T=400, d=512, E=16, k=4, I=256, R=4)),
-    ("e4m3 experts, one-SM tiles", mi.config(4).scaled(T=40, d=512, E=64, k=4, I=256, R=8)),
+     mi.config("prefill_bf16_skew_eplb").scaled(T=260, d=256, E=16, k=4, I=256, R=4, n_redundant=4,
+                                                expert_placement=1)),
+    ("e4m3 experts, pair tiles", mi.config("prefill_fp8_skew").scaled(T=400, d=512, E=16, k=4, I=256, R=4)),
+    ("e4m3 experts, one-SM tiles", mi.config("prefill_fp8_skew").scaled(T=40, d=512, E=64, k=4, I=256, R=8)),
 ]
 
 
@@ -94,7 +96,7 @@ def test_layer_writes_stay_inside_buffers_and_repeat_exactly(name, cfg):
 
 
 def test_fused_entry_points_write_inside_their_buffers():
-    cfg = mi.config(2).scaled(T=300, d=384, E=16, k=4, I=256, R=4)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=300, d=384, E=16, k=4, I=256, R=4)
     ids, tw = O.route(mi.make_logits(cfg), cfg.k)
     lay = O.dispatch_layout(ids, cfg.E, cfg.R, None)
     N, T = cfg.N, cfg.T

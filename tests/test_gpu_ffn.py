@@ -68,7 +68,7 @@ def run_ffn(cfg, mode, logits=None, eplb=False):
     return lay
 
 
-SMALL = mi.config(2).scaled(T=100, d=256, E=8, I=256, R=4, shared=False, zipf_bias=False)
+SMALL = mi.config("prefill_bf16_skew").scaled(T=100, d=256, E=8, I=256, R=4, shared=False, zipf_bias=False)
 
 
 @pytest.mark.parametrize("mode", ["swap", "wide", "pair"])

@@ -74,7 +74,7 @@ def run_ffn_fp8(cfg, logits=None, mode=None):
     return check_rms(got, ref)
 
 
-SMALL = mi.config(4).scaled(T=300, d=256, E=8, I=256, R=4)
+SMALL = mi.config("prefill_fp8_skew").scaled(T=300, d=256, E=8, I=256, R=4)
 MODES = ["wide", "pair"]      # one-SM tiles, SM-pair tiles
 
 

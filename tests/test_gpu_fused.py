@@ -97,7 +97,7 @@ def run_gather(cfg, logits=None, eplb=False):
     return lay
 
 
-SMALL = mi.config(2).scaled(T=100, d=256, E=8, I=256, R=4, shared=False, zipf_bias=False)
+SMALL = mi.config("prefill_bf16_skew").scaled(T=100, d=256, E=8, I=256, R=4, shared=False, zipf_bias=False)
 
 
 def test_gather_small():
@@ -129,7 +129,7 @@ def test_gather_single_token():
 
 def test_gather_deep_k_wraps_the_stage_ring():
     # d = 1024: 16 K blocks per tile, so the operand stages wrap within and across tiles
-    cfg = mi.config(2).scaled(T=1500, d=1024, E=32, k=8, I=512, R=4, shared=True)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=1500, d=1024, E=32, k=8, I=512, R=4, shared=True)
     lay = run_gather(cfg)
     assert np.diff(lay["phys_offsets"]).max() > 128
 
@@ -254,5 +254,5 @@ def test_combine_single_token_and_k_one():
 
 
 def test_combine_many_tiles():
-    cfg = mi.config(2).scaled(T=1500, d=1024, E=32, k=8, I=512, R=4, shared=True)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=1500, d=1024, E=32, k=8, I=512, R=4, shared=True)
     run_combine(cfg)

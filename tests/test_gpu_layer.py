@@ -124,21 +124,21 @@ def check(cfg, sample=None, bias=None):
 
 
 def test_layer_tiny_fp32_full():
-    check(mi.config(0))
+    check(mi.config("tiny_fp32"))
 
 
 @pytest.mark.parametrize("T", [1, 3, 65])
 def test_layer_tiny_fp32_ragged(T):
-    check(mi.config(0).scaled(T=T))
+    check(mi.config("tiny_fp32").scaled(T=T))
 
 
 def test_device_generator_matches_host():
-    for ci in (1, 4):
-        cfg = mi.config(ci)
+    for workload in ("decode_bf16", "prefill_fp8_skew"):
+        cfg = mi.config(workload)
         for which, e in (("w_gate", 0), ("w_down", 255)):
             dev = host_bf16_bits(mi.make_weight_device(cfg, which, e, "cuda"))
             assert np.array_equal(dev, mi.make_weight_host(cfg, which, e))
-    cfg = mi.config(2)
+    cfg = mi.config("prefill_bf16_skew")
     dev = host_bf16_bits(mi.make_weight_device(cfg, "ws_up", 0, "cuda"))
     assert np.array_equal(dev, mi.make_weight_host(cfg, "ws_up", 0))
 
@@ -149,21 +149,21 @@ def test_layer_bf16_degenerate_routing(kw):
     # a single token
     base = dict(T=300, d=256, I=256, shared=False, zipf_bias=False)
     base.update(kw)
-    check(mi.config(2).scaled(**base))
+    check(mi.config("prefill_bf16_skew").scaled(**base))
 
 
 # ------------------------------------------------------------------ bf16 workloads
 def test_layer_bf16_small_full():
-    check(mi.config(2).scaled(T=200, d=256, E=16, I=256, R=4))
+    check(mi.config("prefill_bf16_skew").scaled(T=200, d=256, E=16, I=256, R=4))
 
 
 def test_layer_bf16_small_eplb_full():
-    check(mi.config(3).scaled(T=200, d=256, E=16, I=256, R=4, n_redundant=4))
+    check(mi.config("prefill_bf16_skew_eplb").scaled(T=200, d=256, E=16, I=256, R=4, n_redundant=4))
 
 
 def test_layer_bf16_small_balanced_eplb_full():
     # the load-aware placement: the hottest experts take several replicas; P % R only
-    check(mi.config(3).scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1))
+    check(mi.config("prefill_bf16_skew_eplb").scaled(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1))
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(n_redundant=4), dict(n_redundant=8, eplb_placement=1)])
@@ -172,13 +172,13 @@ def test_layer_bf16_small_round_robin(kw):
     # replicas, and with the load-aware map (only the "before" statistics change)
     base = dict(T=300, d=256, E=16, I=256, R=4, n_redundant=0, expert_placement=1)
     base.update(kw)
-    check(mi.config(3).scaled(**base))
+    check(mi.config("prefill_bf16_skew_eplb").scaled(**base))
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(shared=True, n_redundant=4)])
 def test_layer_bf16_small_fp8_dispatch(kw):
     # tokens dispatched as e4m3 with per-128-channel scales, bf16 rows rebuilt for the experts
-    check(mi.config(2).scaled(T=300, d=256, E=16, I=256, R=4, shared=False, fp8_dispatch=1).scaled(**kw))
+    check(mi.config("prefill_bf16_skew").scaled(T=300, d=256, E=16, I=256, R=4, shared=False, fp8_dispatch=1).scaled(**kw))
 
 
 @pytest.mark.parametrize("kw", [dict(T=1), dict(T=37, d=128, I=128), dict(T=64, E=4, k=4, R=4, expert_placement=1),
@@ -188,7 +188,7 @@ def test_layer_bf16_edge_cases_new_options(kw):
     # round-robin placement — with the FP8 dispatch on
     base = dict(T=300, d=256, E=16, I=256, R=4, shared=False, zipf_bias=False, fp8_dispatch=1)
     base.update(kw)
-    check(mi.config(2).scaled(**base))
+    check(mi.config("prefill_bf16_skew").scaled(**base))
 
 
 @pytest.mark.parametrize("kw", [dict(T=64, E=32, k=8), dict(T=65, E=32, k=8), dict(T=32, E=64, k=8),
@@ -200,26 +200,27 @@ def test_layer_single_launch_route_and_layout_bounds(kw):
     # of the bound
     base = dict(T=300, d=128, E=16, k=8, I=128, R=4, shared=False, zipf_bias=False)
     base.update(kw)
-    check(mi.config(2).scaled(**base))
+    check(mi.config("prefill_bf16_skew").scaled(**base))
 
 
 def test_layer_prefill_bf16_skew_fp8_dispatch():
-    cfg = mi.config(2).scaled(fp8_dispatch=1)
+    cfg = mi.config("prefill_bf16_skew").scaled(fp8_dispatch=1)
     check(cfg, sample=tile_sample(cfg, mi.make_logits(cfg), seed=2))
 
 
 def test_layer_fp8_experts_ignore_fp8_dispatch():
-    cfg = mi.config(4).scaled(T=300, d=256, E=8, I=256, R=4)
+    cfg = mi.config("prefill_fp8_skew").scaled(T=300, d=256, E=8, I=256, R=4)
     a = run_layer(cfg)[3]
     b = run_layer(cfg.scaled(fp8_dispatch=1))[3]
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("ci,kw", [(0, dict()), (2, dict(T=300, d=256, E=16, I=256, R=4))])
-def test_layer_selection_bias(ci, kw):
+@pytest.mark.parametrize("workload,kw", [("tiny_fp32", dict()),
+                                         ("prefill_bf16_skew", dict(T=300, d=256, E=16, I=256, R=4))])
+def test_layer_selection_bias(workload, kw):
     # experts picked by logit + bias, weighted by the unbiased logits; the bias moves
     # the hottest expert's tokens elsewhere
-    cfg = mi.config(ci).scaled(**kw)
+    cfg = mi.config(workload).scaled(**kw)
     bias = np.linspace(-2.0, 1.0, cfg.E).astype(np.float32)
     layer, ref = check(cfg, bias=bias)
     plain = O.route(mi.make_logits(cfg), cfg.k)[0]
@@ -227,31 +228,31 @@ def test_layer_selection_bias(ci, kw):
 
 
 def test_layer_decode_bf16():
-    check(mi.config(1))                                   # all 128 tokens
+    check(mi.config("decode_bf16"))                                   # all 128 tokens
 
 
 def test_layer_prefill_bf16_skew():
-    cfg = mi.config(2)
+    cfg = mi.config("prefill_bf16_skew")
     check(cfg, sample=tile_sample(cfg, mi.make_logits(cfg)))
 
 
 def test_layer_prefill_bf16_skew_eplb():
-    cfg = mi.config(3)
+    cfg = mi.config("prefill_bf16_skew_eplb")
     check(cfg, sample=tile_sample(cfg, mi.make_logits(cfg), seed=1))
 
 
 def test_layer_prefill_bf16_skew_load_aware_eplb():
-    cfg = mi.config(3).scaled(eplb_placement=1)
+    cfg = mi.config("prefill_bf16_skew_eplb").scaled(eplb_placement=1)
     check(cfg, sample=tile_sample(cfg, mi.make_logits(cfg), seed=3))
 
 
 # ------------------------------------------------------------------ fp8 workload
 def test_layer_fp8_small_full():
-    check(mi.config(4).scaled(T=200, d=256, E=16, I=256, R=4))
+    check(mi.config("prefill_fp8_skew").scaled(T=200, d=256, E=16, I=256, R=4))
 
 
 def test_layer_prefill_fp8_skew():
-    cfg = mi.config(4)
+    cfg = mi.config("prefill_fp8_skew")
     check(cfg, sample=tile_sample(cfg, mi.make_logits(cfg), seed=2))
 
 
@@ -270,7 +271,7 @@ def test_layer_forward_replays_in_a_cuda_graph(name, kw):
     captured buffers give exactly what eager calls give."""
     kw = dict(kw)
     bias = kw.pop("bias", False)
-    cfg = mi.config(2).scaled(**{"shared": False, "zipf_bias": False, "dtype": "bf16", **kw})
+    cfg = mi.config("prefill_bf16_skew").scaled(**{"shared": False, "zipf_bias": False, "dtype": "bf16", **kw})
     act = moe.MOE_BF16
     ex = dtype_code(cfg.dtype)
     pw = PackedWeights(cfg.E, cfg.d, cfg.I, ex, cfg.shared,

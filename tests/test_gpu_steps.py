@@ -58,9 +58,9 @@ def check_route(logits, k):
     assert nbad == 0, mx
 
 
-@pytest.mark.parametrize("ci", range(5))
-def test_route_workloads(ci):
-    cfg = mi.config(ci)
+@pytest.mark.parametrize("workload", mi.NAMES)
+def test_route_workloads(workload):
+    cfg = mi.config(workload)
     check_route(mi.make_logits(cfg), cfg.k)
 
 
@@ -140,9 +140,9 @@ def check_layout(ids, E, R, eplb=None, placement="linear"):
     return g, r
 
 
-@pytest.mark.parametrize("ci", range(5))
-def test_layout_workloads(ci):
-    cfg = mi.config(ci)
+@pytest.mark.parametrize("workload", mi.NAMES)
+def test_layout_workloads(workload):
+    cfg = mi.config(workload)
     ids, _ = O.route(mi.make_logits(cfg), cfg.k)
     emap = None
     if cfg.n_redundant:
@@ -355,9 +355,10 @@ def test_layout_with_balanced_map(T, E, R, n_red):
     check_layout(ids, E, R, emap)
 
 
-@pytest.mark.parametrize("ci,T", [(0, None), (1, None), (2, 1024), (4, 512)])
-def test_permute_copy_is_exact(ci, T):
-    cfg = mi.config(ci) if T is None else mi.config(ci).scaled(T=T)
+@pytest.mark.parametrize("workload,T", [("tiny_fp32", None), ("decode_bf16", None), ("prefill_bf16_skew", 1024),
+                                        ("prefill_fp8_skew", 512)])
+def test_permute_copy_is_exact(workload, T):
+    cfg = mi.config(workload) if T is None else mi.config(workload).scaled(T=T)
     ids, w, lay = layout_for(cfg)
     x = mi.make_x(cfg)
     dt = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
@@ -373,7 +374,7 @@ def test_permute_copy_is_exact(ci, T):
 
 @pytest.mark.parametrize("T,d", [(16384, 6144), (37, 128), (5, 384)])
 def test_permute_e4m3_codes_exact(T, d):
-    cfg = mi.config(4).scaled(T=T, d=d)
+    cfg = mi.config("prefill_fp8_skew").scaled(T=T, d=d)
     ids, w, lay = layout_for(cfg)
     x = mi.make_x(cfg)
     # add scale variety and exact zeros per group
@@ -391,11 +392,11 @@ def test_permute_e4m3_codes_exact(T, d):
     assert np.array_equal(sc.cpu().numpy(), s[r2t])
 
 
-@pytest.mark.parametrize("ci,T", [(0, None), (1, None), (2, 2048)])
-def test_combine_and_identity_experts(ci, T):
-    cfg = mi.config(ci) if T is None else mi.config(ci).scaled(T=T)
+@pytest.mark.parametrize("workload,T", [("tiny_fp32", None), ("decode_bf16", None), ("prefill_bf16_skew", 2048)])
+def test_combine_and_identity_experts(workload, T):
+    cfg = mi.config(workload) if T is None else mi.config(workload).scaled(T=T)
     ids, w, lay = layout_for(cfg)
-    rng = np.random.default_rng(ci)
+    rng = np.random.default_rng(mi.NAMES.index(workload))
     y = rng.standard_normal((cfg.N, cfg.d)).astype(np.float32)
     sh = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
     dt = moe.MOE_F32 if cfg.dtype == "fp32" else moe.MOE_BF16
@@ -460,7 +461,7 @@ def packed_bytes(t):
 @pytest.mark.parametrize("dst", ["bf16", "fp8", "fp32"])
 def test_pack_weights(dst):
     d, I = 256, 384
-    cfg = mi.config(1).scaled(d=d, I=I, dtype="fp32" if dst == "fp32" else "bf16")
+    cfg = mi.config("decode_bf16").scaled(d=d, I=I, dtype="fp32" if dst == "fp32" else "bf16")
     code = {"bf16": moe.MOE_BF16, "fp8": moe.MOE_E4M3, "fp32": moe.MOE_F32}[dst]
     pw = PackedWeights(2, d, I, code, False)
     wg, wu, wd = (mi.make_weight_host(cfg, n, 1) for n in ("w_gate", "w_up", "w_down"))

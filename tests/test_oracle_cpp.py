@@ -56,24 +56,26 @@ def assert_same_layer(a, b):
 
 
 CASES = [
-    ("tiny_fp32", 0, dict()),
-    ("tiny_fp32, round-robin", 0, dict(expert_placement=1)),
-    ("tiny_fp32, ragged", 0, dict(T=37)),
-    ("decode-shaped bf16", 1, dict(d=256, I=256, E=32, R=8)),
-    ("prefill bf16 + shared", 2, dict(T=300, d=256, E=16, I=256, R=4)),
-    ("prefill bf16 + EPLB", 3, dict(T=300, d=256, E=16, I=256, R=4, n_redundant=4)),
-    ("prefill bf16 + load-aware EPLB", 3, dict(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1)),
-    ("prefill bf16 + EPLB, round-robin", 3, dict(T=300, d=256, E=16, I=256, R=4, n_redundant=4, expert_placement=1)),
-    ("prefill bf16, FP8 dispatch", 2, dict(T=300, d=256, E=16, I=256, R=4, fp8_dispatch=1)),
-    ("fp8 experts", 4, dict(T=300, d=256, E=16, I=256, R=4)),
-    ("degenerate E = k = 1", 2, dict(T=50, d=128, E=1, k=1, I=128, R=1, shared=False)),
-    ("k = E", 2, dict(T=50, d=128, E=8, k=8, I=128, R=4, shared=False)),
+    ("tiny_fp32", "tiny_fp32", dict()),
+    ("tiny_fp32, round-robin", "tiny_fp32", dict(expert_placement=1)),
+    ("tiny_fp32, ragged", "tiny_fp32", dict(T=37)),
+    ("decode-shaped bf16", "decode_bf16", dict(d=256, I=256, E=32, R=8)),
+    ("prefill bf16 + shared", "prefill_bf16_skew", dict(T=300, d=256, E=16, I=256, R=4)),
+    ("prefill bf16 + EPLB", "prefill_bf16_skew_eplb", dict(T=300, d=256, E=16, I=256, R=4, n_redundant=4)),
+    ("prefill bf16 + load-aware EPLB", "prefill_bf16_skew_eplb",
+     dict(T=300, d=256, E=16, I=256, R=4, n_redundant=8, eplb_placement=1)),
+    ("prefill bf16 + EPLB, round-robin", "prefill_bf16_skew_eplb",
+     dict(T=300, d=256, E=16, I=256, R=4, n_redundant=4, expert_placement=1)),
+    ("prefill bf16, FP8 dispatch", "prefill_bf16_skew", dict(T=300, d=256, E=16, I=256, R=4, fp8_dispatch=1)),
+    ("fp8 experts", "prefill_fp8_skew", dict(T=300, d=256, E=16, I=256, R=4)),
+    ("degenerate E = k = 1", "prefill_bf16_skew", dict(T=50, d=128, E=1, k=1, I=128, R=1, shared=False)),
+    ("k = E", "prefill_bf16_skew", dict(T=50, d=128, E=8, k=8, I=128, R=4, shared=False)),
 ]
 
 
-@pytest.mark.parametrize("name,ci,kw", CASES, ids=[c[0] for c in CASES])
-def test_cpp_layer_equals_numpy(name, ci, kw):
-    cfg = mi.config(ci).scaled(**kw)
+@pytest.mark.parametrize("name,workload,kw", CASES, ids=[c[0] for c in CASES])
+def test_cpp_layer_equals_numpy(name, workload, kw):
+    cfg = mi.config(workload).scaled(**kw)
     logits, x = mi.make_logits(cfg), mi.make_x(cfg)
     w = host_weights(cfg)
     a = NP.layer_forward(cfg, logits, x, w)
@@ -83,7 +85,7 @@ def test_cpp_layer_equals_numpy(name, ci, kw):
 
 
 def test_cpp_layer_token_subset_and_selection_bias():
-    cfg = mi.config(2).scaled(T=300, d=256, E=16, I=256, R=4)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=300, d=256, E=16, I=256, R=4)
     logits, x = mi.make_logits(cfg), mi.make_x(cfg)
     w = host_weights(cfg)
     toks = np.array([0, 7, 150, 299])
@@ -96,7 +98,7 @@ def test_cpp_layer_token_subset_and_selection_bias():
 
 
 def test_cpp_layer_threads_do_not_change_results():
-    cfg = mi.config(4).scaled(T=300, d=256, E=16, I=256, R=4)
+    cfg = mi.config("prefill_fp8_skew").scaled(T=300, d=256, E=16, I=256, R=4)
     logits, x = mi.make_logits(cfg), mi.make_x(cfg)
     w = host_weights(cfg)
     one = CPP.layer_forward(cfg, logits, x, w, threads=1)
@@ -105,7 +107,7 @@ def test_cpp_layer_threads_do_not_change_results():
 
 
 def test_cpp_layer_rejects_bad_input():
-    cfg = mi.config(0)
+    cfg = mi.config("tiny_fp32")
     logits, x = mi.make_logits(cfg), mi.make_x(cfg)
     logits[3, 1] = np.inf
     with pytest.raises(ValueError):

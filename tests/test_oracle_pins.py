@@ -121,7 +121,7 @@ def test_route_k1_is_argmax_weight_one():
 
 
 def test_route_weights_two_forms_agree():
-    l = mi.make_logits(mi.config(0))
+    l = mi.make_logits(mi.config("tiny_fp32"))
     _, w1 = O.route(l, 2)
     _, w2 = O.route_softmax_then_renorm(l, 2)
     np.testing.assert_allclose(w1, w2, rtol=0, atol=1e-12)
@@ -313,7 +313,7 @@ def test_eplb_map_geometry_and_hot_list():
 
 
 def test_eplb_token_split_by_parity():
-    cfg = mi.config(3).scaled(T=512)
+    cfg = mi.config("prefill_bf16_skew_eplb").scaled(T=512)
     l = mi.make_logits(cfg)
     ids, _ = O.route(l, cfg.k)
     m = O.eplb_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.R, cfg.n_redundant)
@@ -388,7 +388,7 @@ def test_round_robin_layout_brute_force(T, E, k, R):
 
 def test_round_robin_layer_output_equals_linear():
     """The placement moves rows between ranks; the layer's result is unchanged."""
-    cfg = mi.config(0)
+    cfg = mi.config("tiny_fp32")
     l = mi.make_logits(cfg)
     x = np.random.default_rng(3).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 4)
@@ -462,7 +462,7 @@ def test_fp8_dispatch_lossless_on_the_e4m3_grid():
     """Tokens whose 128-channel groups hold e4m3 values times 2^-4 with amax 28 have
     scale 2^-4 exactly, so the e4m3 dispatch returns them unchanged and the layer's
     output equals the plain bf16 dispatch's."""
-    cfg = mi.config(2).scaled(T=24, d=256, E=4, k=2, I=128, R=2, shared=False, zipf_bias=False)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=24, d=256, E=4, k=2, I=128, R=2, shared=False, zipf_bias=False)
     rng = np.random.default_rng(12)
     grid = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))            # finite non-negative values
     x = (rng.choice(grid, size=(cfg.T, cfg.d)) * rng.choice([-1.0, 1.0], size=(cfg.T, cfg.d)) / 16.0)
@@ -499,7 +499,7 @@ def test_fp8_dispatch_lossless_on_the_e4m3_grid():
 
 
 def test_layer_selection_bias_special_cases():
-    cfg = mi.config(0)
+    cfg = mi.config("tiny_fp32")
     l = mi.make_logits(cfg)
     x = np.random.default_rng(14).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 15)
@@ -545,7 +545,7 @@ def tiny_weights(cfg, seed):
 
 
 def test_ffn_single_expert_is_dense_swiglu():
-    cfg = mi.config(0).scaled(E=1, k=1, R=1)
+    cfg = mi.config("tiny_fp32").scaled(E=1, k=1, R=1)
     x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 9)
     res = O.layer_forward(cfg, np.zeros((cfg.T, 1), np.float32), x, wt)
@@ -554,7 +554,7 @@ def test_ffn_single_expert_is_dense_swiglu():
 
 
 def test_ffn_top1_uses_argmax_expert():
-    cfg = mi.config(0).scaled(k=1)
+    cfg = mi.config("tiny_fp32").scaled(k=1)
     rng = np.random.default_rng(10)
     x = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
     l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
@@ -568,7 +568,7 @@ def test_ffn_top1_uses_argmax_expert():
 
 
 def test_ffn_all_experts_softmax_mixture_with_shared():
-    cfg = mi.config(0).scaled(k=8, shared=True, T=8)
+    cfg = mi.config("tiny_fp32").scaled(k=8, shared=True, T=8)
     rng = np.random.default_rng(12)
     x = rng.standard_normal((cfg.T, cfg.d)).astype(np.float32)
     l = rng.standard_normal((cfg.T, cfg.E)).astype(np.float32)
@@ -582,7 +582,7 @@ def test_ffn_all_experts_softmax_mixture_with_shared():
 
 
 def test_identity_experts_return_x():
-    cfg = mi.config(0)
+    cfg = mi.config("tiny_fp32")
     x = mi.make_x(cfg).astype(np.float64)
     ids, w = O.route(mi.make_logits(cfg), cfg.k)
     lay = O.dispatch_layout(ids, cfg.E, cfg.R)
@@ -593,7 +593,7 @@ def test_identity_experts_return_x():
 
 def test_dispatch_bytes_and_expert_size_arithmetic():
     g = load("expert_arithmetic.json")
-    cfg = mi.config(1)
+    cfg = mi.config("decode_bf16")
     assert 3 * cfg.d * cfg.I == g["expert_params_glm"]
     assert round(3 * cfg.d * cfg.I / 1e6, 1) == g["expert_mb_fp8_glm"]   # one byte per e4m3 weight
     T = 4
@@ -694,8 +694,8 @@ def test_bf16_bracket_by_hand():
 
 
 def test_layer_envelope_holds_the_round_to_nearest_output():
-    for cfg in (mi.config(2).scaled(T=40, d=128, E=8, I=128, R=4), mi.config(0),
-                mi.config(4).scaled(T=40, d=128, E=8, I=128, R=4)):
+    for cfg in (mi.config("prefill_bf16_skew").scaled(T=40, d=128, E=8, I=128, R=4), mi.config("tiny_fp32"),
+                mi.config("prefill_fp8_skew").scaled(T=40, d=128, E=8, I=128, R=4)):
         x = mi.make_x(cfg)
         l = mi.make_logits(cfg)
         wt = tiny_weights(cfg, 17)
@@ -712,7 +712,7 @@ def test_layer_envelope_holds_the_round_to_nearest_output():
 def test_layer_envelope_by_hand():
     # one token, E = k = 1 with weight 1, d = 1: y = h w_down = 1 + 2^-8 exactly (the
     # bf16 tie), so the envelope is [1, 1 + 2^-7] and the rounded output 1
-    cfg = mi.config(2).scaled(T=1, d=128, E=1, k=1, I=128, R=1, shared=False, zipf_bias=False)
+    cfg = mi.config("prefill_bf16_skew").scaled(T=1, d=128, E=1, k=1, I=128, R=1, shared=False, zipf_bias=False)
     wg = np.zeros((128, 128), np.float32)
     wu = np.zeros((128, 128), np.float32)
     wd = np.zeros((128, 128), np.float32)
@@ -732,7 +732,7 @@ def test_pins_catch_planted_mistakes(monkeypatch, oracle_impl):
     (the C++ oracle's planted slips are compiled variants: test_oracle_cpp.py)."""
     if oracle_impl != "numpy":
         pytest.skip("monkeypatched slips are for the numpy oracle")
-    cfg = mi.config(0).scaled(E=1, k=1, R=1)
+    cfg = mi.config("tiny_fp32").scaled(E=1, k=1, R=1)
     x = np.random.default_rng(8).standard_normal((cfg.T, cfg.d)).astype(np.float32)
     wt = tiny_weights(cfg, 9)
     ref = torch_swiglu(x, wt("w_gate", 0), wt("w_up", 0), wt("w_down", 0)).numpy()

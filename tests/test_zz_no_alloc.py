@@ -42,8 +42,8 @@ def run_layout(static, ids_np, E, R, eplb_np=None):
     return res
 
 
-def case(ci, T=None, eplb=False):
-    cfg = mi.config(ci) if T is None else mi.config(ci).scaled(T=T)
+def case(workload, T=None, eplb=False):
+    cfg = mi.config(workload) if T is None else mi.config(workload).scaled(T=T)
     ids, _ = O.route(mi.make_logits(cfg), cfg.k)
     emap = O.eplb_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.R, cfg.n_redundant) if eplb else None
     return ids, cfg.E, cfg.R, emap
@@ -52,7 +52,8 @@ def case(ci, T=None, eplb=False):
 def test_static_scratch_layout_matches_workspace_layout_call_after_call():
     # a large skewed batch with EPLB, then a small decode batch, then the large one
     # again: each call overwrites what the previous one left in the shared scratch
-    cases = [case(3, eplb=True), case(1), case(4, T=4096), case(3, eplb=True)]
+    cases = [case("prefill_bf16_skew_eplb", eplb=True), case("decode_bf16"), case("prefill_fp8_skew", T=4096),
+             case("prefill_bf16_skew_eplb", eplb=True)]
     for ids, E, R, emap in cases:
         ref = run_layout(False, ids, E, R, emap)
         got = run_layout(True, ids, E, R, emap)
