@@ -307,3 +307,44 @@ def test_layer_forward_replays_in_a_cuda_graph(name, kw):
         torch.cuda.synchronize()
         assert int(layer.err.item()) == 0
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), name
+
+
+def sweep_configs(n=16, seed=2024):
+    """Seeded random small layers: every option of the layer, mixed, with ragged
+    batches (bf16 experts with or without the shared expert, both EPLB placements,
+    the round-robin base placement, FP8 dispatch; e4m3 experts)."""
+    rng = np.random.default_rng(seed)
+    cfgs = []
+    for i in range(n):
+        fp8 = i % 4 == 3
+        E = int(rng.choice([8, 16, 32, 64]))
+        R = int(rng.choice([r for r in (1, 2, 4, 8) if E % r == 0]))
+        k = int(rng.integers(1, min(8, E) + 1))
+        T = int(rng.integers(1, 400))
+        if fp8:
+            d, I, shared = int(rng.choice([256, 512])), int(rng.choice([128, 256])), False
+        else:
+            d, I = int(rng.choice([128, 256, 384])), int(rng.choice([128, 256, 384]))
+            shared = bool(rng.integers(0, 2))
+        n_red, placement = 0, 0
+        if not fp8 and rng.random() < 0.5:
+            placement = int(rng.integers(0, 2))
+            n_red = R * int(rng.integers(1, (E // R if placement == 0 else 2 * E // R) + 1))
+        cfgs.append(mi.config("prefill_bf16_skew").scaled(
+            name=f"sweep{i}", T=T, d=d, E=E, k=k, I=I, R=R, shared=shared, n_redundant=n_red,
+            eplb_placement=placement, expert_placement=int(rng.random() < 0.3),
+            fp8_dispatch=int(not fp8 and rng.random() < 0.3), zipf_bias=bool(rng.integers(0, 2)),
+            dtype="fp8" if fp8 else "bf16", seed=100 + i))
+    return cfgs
+
+
+SWEEP = sweep_configs()
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=[
+    f"{c.name}-T{c.T}-d{c.d}-E{c.E}-k{c.k}-I{c.I}-R{c.R}-{c.dtype}{'-shared' if c.shared else ''}"
+    f"{f'-eplb{c.n_redundant}p{c.eplb_placement}' if c.n_redundant else ''}{'-rr' if c.expert_placement else ''}"
+    f"{'-fp8dispatch' if c.fp8_dispatch else ''}" for c in SWEEP])
+def test_layer_random_small_configs(cfg):
+    # every output of every token against the oracle
+    check(cfg)
