@@ -13,7 +13,7 @@ import moe_inputs as mi
 from combine_softmax_top_expert_b300.layer import PackedWeights
 from oracle import moe_oracle as O
 
-from _util import FP8_RMS, fill_weights
+from _util import FP8_CONSISTENCY, FP8_RMS, fill_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,9 @@ def rms(a):
 def check_rms(got, ref, per_row=True):
     assert np.all(np.isfinite(got))
     err = rms(got - ref)
+    print(f"rms error / rms(out) = {err / rms(ref):.3e}")
     assert err <= FP8_RMS * rms(ref), (err, rms(ref))
+    assert err <= FP8_CONSISTENCY * rms(ref), (err, rms(ref))
     if per_row:
         row_err = np.sqrt(np.mean((got - ref) ** 2, axis=1))
         row_ref = np.sqrt(np.mean(ref ** 2, axis=1))

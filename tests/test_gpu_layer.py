@@ -16,7 +16,8 @@ import moe_inputs as mi
 from combine_softmax_top_expert_b300.layer import Layer, PackedWeights, dtype_code
 from oracle import cpp_oracle
 
-from _util import BF16_TOL, F32_TOL, FP8_RMS, close, dev_f32, dev_x, fill_weights, host_bf16_bits
+from _util import (BF16_TOL, F32_TOL, FP8_CONSISTENCY, FP8_RMS, close, dev_f32, dev_x, fill_weights,
+                   host_bf16_bits)
 
 pytestmark = pytest.mark.gpu
 O = cpp_oracle.default()
@@ -103,6 +104,7 @@ def check(cfg, sample=None, bias=None):
         print(f"{cfg.name}: {len(toks)} tokens, rms error / rms(out) = {ratio:.3e} (worst token {per_row.max():.3e});"
               f" bound {FP8_RMS}")
         assert ratio <= FP8_RMS and per_row.max() <= FP8_RMS, (ratio, per_row.max())
+        assert ratio <= FP8_CONSISTENCY, ratio
     elif cfg.dtype == "fp32":
         nbad, mx = close(got, ref["out"], F32_TOL)
         assert nbad == 0, (nbad, mx)
