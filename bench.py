@@ -54,7 +54,9 @@ def parse():
     ap.add_argument("--workload", default="prefill_fp8_skew")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=256, help="tokens in the CPU-baseline sample")
-    ap.add_argument("--ref-tokens", type=int, default=2, help="tokens per step of the reference arm")
+    ap.add_argument("--ref-tokens", type=int, default=2,
+                    help="tokens per step of the reference arm (1 when more than 40 steps are asked for, so the "
+                         "run stays within a few minutes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compare-fused", action="store_true",
                     help="bf16 workloads: time the two fused expert-FFN entry points against the separate steps "
@@ -615,7 +617,9 @@ def run_reference(args, world, rank):
     except Exception:
         dev = None
     weight = oracle_weights(cfg, dev)
-    per_step = max(1, min(args.ref_tokens, cfg.T))
+    # about 1.6 s of oracle work per sampled token (mostly preparing the weights of the
+    # experts it picks): long runs sample one token per step
+    per_step = max(1, min(args.ref_tokens if args.steps <= 40 else 1, cfg.T))
 
     def step(i):
         # a different strided sample each step: tokens i, i + T/n, ...
