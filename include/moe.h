@@ -435,9 +435,12 @@ moe_status_t moe_expert_down(const void *h, const float *h_scales,
  * writes; topk_w [T, k] fp32; T_shared is 0 or T (the shared expert's rows, from
  * moe_expert_gate_up, follow the routed ones in h); counts is caller scratch of
  * T * (d / 128) int32, overwritten.  k <= 32; always runs the one-SM tiles of 128
- * token rows; y_perm and out 16-byte aligned.  Returns MOE_ERR_UNSUPPORTED for
- * other weight dtypes.  A row whose token is outside [0, T) sets MOE_DEV_LAYOUT and
- * leaves that token's out unspecified. */
+ * token rows; y_perm and out 16-byte aligned.  A block can only be summed after its
+ * last row, so most sums fall at the end of the launch: on prefill batches this
+ * measured slower than moe_expert_down followed by moe_combine, and the layer
+ * forward does not use it.  Returns MOE_ERR_UNSUPPORTED for other weight dtypes.  A
+ * row whose token is outside [0, T) sets MOE_DEV_LAYOUT and leaves that token's out
+ * unspecified. */
 moe_status_t moe_expert_down_combine(const void *h, const int32_t *phys_offsets, int64_t P,
                                      const int32_t *phys_to_logical, int64_t rows_hint,
                                      const moe_weights_t *w, int64_t T_shared,
