@@ -125,3 +125,49 @@ def test_ffn_smallest_dims(mode):
     # d = I = 128: one K block and one feature tile in every GEMM (d < 256, so the pair
     # orientation's down projection runs on one-SM tiles)
     run_ffn(SMALL.scaled(T=50, d=128, I=128, E=4, k=2, R=2, shared=True), mode)
+
+
+@pytest.mark.parametrize("eplb", [False, True], ids=["linear", "eplb"])
+@pytest.mark.parametrize("mode", ["swap", "wide", "pair"])
+def test_ffn_per_rank_slices_equal_the_whole(mode, eplb):
+    # the layout orders rows by (rank, expert): each logical rank's slice of x_perm,
+    # with its own experts' offsets, runs on its own and gives exactly the rows the
+    # whole batch gives them -- what an expert-parallel deployment would run per GPU
+    cfg = SMALL.scaled(T=300, E=16, k=4, R=4, n_redundant=4 if eplb else 0, zipf_bias=True)
+    ids, _ = O.route(mi.make_logits(cfg), cfg.k)
+    emap = O.eplb_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.R, cfg.n_redundant) if eplb else None
+    lay = O.dispatch_layout(ids, cfg.E, cfg.R, emap)
+    P, N = lay["P"], cfg.N
+    p2l_all = emap["phys_to_logical"] if eplb else np.arange(P, dtype=np.int32)
+    po = lay["phys_offsets"].astype(np.int64)
+    xp = dev_bf16(O.permute(mi.make_x(cfg), lay["row_to_token"]))
+    pw = PackedWeights(cfg.E, cfg.d, cfg.I, moe.MOE_BF16, False)
+    fill_weights(cfg, pw)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def ffn(x_rows, offs, n_phys, p2l, rows):
+        y = torch.full((max(rows, 1), cfg.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        wsb = moe.moe_ffn_workspace_size(rows, cfg.I, moe.MOE_BF16)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        moe.moe_expert_ffn(x_rows, None, i32(offs), n_phys, i32(p2l), rows, pw.struct(), None, 0, y, ws, wsb, err)
+        return y
+
+    os.environ["MOE_B300_FFN_TILES"] = mode
+    try:
+        whole = ffn(xp, po, P, p2l_all, N)
+        per = P // cfg.R
+        slices = []
+        for r in range(cfg.R):
+            a, b = int(po[r * per]), int(po[(r + 1) * per])
+            assert a == lay["rank_offsets"][r] and b == lay["rank_offsets"][r + 1]
+            if b > a:
+                slices.append((a, b, ffn(xp[a:b], po[r * per:(r + 1) * per + 1] - a, per,
+                                         p2l_all[r * per:(r + 1) * per], b - a)))
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["MOE_B300_FFN_TILES"]
+    assert int(err.item()) == 0
+    assert len(slices) > 1
+    for a, b, y in slices:
+        assert torch.equal(y[:b - a].view(torch.int16), whole[a:b].view(torch.int16))
