@@ -155,10 +155,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       const uint32_t id = idesc(256, 256, 0);
       bool ok = true;
+      // the next block's two barriers are tested right after this block's MMAs, and
+      // the answers read after its commits, so the tests' latency hides behind the
+      // commits (a phase found complete stays complete: the next phase of either
+      // barrier needs a commit this thread has not issued yet)
+      bool pre_full = false, pre_empty = false;
       for (int tile = pair; tile < total && ok; tile += npairs) {
         for (int kb = 0; kb < KB; ++kb, ++gk) {
           const int b = gk & 1;
-          if (!mbar_wait2(full(s), ph, dempty(b), ((gk >> 1) & 1) ^ 1, abort_flag, p.err)) {
+          if (!(pre_full || mbar_wait(full(s), ph, abort_flag, p.err)) ||
+              !(pre_empty || mbar_wait(dempty(b), ((gk >> 1) & 1) ^ 1, abort_flag, p.err))) {
             ok = false;
             break;
           }
@@ -166,12 +172,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a = stage0 + s * kStage, bb = a + kABytes, d = tmem + b * kAccCols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_f8_2(d, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id, kk != 0);
+          const int s1 = s + 1 == kStages ? 0 : s + 1;
+          const uint32_t ph1 = s + 1 == kStages ? ph ^ 1 : ph;
+          pre_full = mbar_test(full(s1), ph1);
+          pre_empty = mbar_test(dempty((gk + 1) & 1), (((gk + 1) >> 1) & 1) ^ 1);
           commit2_both(dfull(b));
           commit2_both(empty(s));
-          if (++s == kStages) {
-            s = 0;
-            ph ^= 1;
-          }
+          s = s1;
+          ph = ph1;
         }
       }
       if (*abort_flag) {  // no MMA may still run when TMEM is freed or the odd CTA leaves

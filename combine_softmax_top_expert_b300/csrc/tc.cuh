@@ -105,15 +105,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Two waits in a row: both phases are tested before either wait suspends, so when
-// both are already complete their latencies overlap.
-__device__ __forceinline__ bool mbar_wait2(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1,
-                                           volatile int *abort_flag, int32_t *err) {
-  const bool done0 = mbar_test(bar0, parity0), done1 = mbar_test(bar1, parity1);
-  if (done0 && done1) return true;
-  return (done0 || mbar_wait(bar0, parity0, abort_flag, err)) && (done1 || mbar_wait(bar1, parity1, abort_flag, err));
-}
-
 // A short bounded wait used only while tearing down after an abort.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
